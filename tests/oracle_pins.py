@@ -1,0 +1,291 @@
+"""Pins for the fp64 oracle: facts fixed by the pages and by the mathematics, not by the
+oracle's own formula.  Each function raises AssertionError when the oracle disagrees.
+
+Sources:
+  [p1] "Kimi K3.1 Pro 架构完全拆解": 3.1 recurrence, 3.2 bounded log-decay, 3.4 replay
+  [p2] "Kimi K3 的架構 ..." (SemiAnalysis translation): 4 delta rule, 6 FlashKDA algorithm
+  [p3] "部署 Kimi K3 ...": 2 segment algebra, 3.3 restart at 2560 = 5 x 512
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from oracle import chunked, segments
+
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def rand_case(T, H, d, seed, decay="sigmoid", s0_std=0.3, beta=None, g=None):
+    rng = np.random.default_rng(seed)
+    def unit(x):
+        return x / np.linalg.norm(x, axis=-1, keepdims=True)
+    q = unit(rng.standard_normal((T, H, d))).astype(np.float32)
+    k = unit(rng.standard_normal((T, H, d))).astype(np.float32)
+    v = rng.standard_normal((T, H, d)).astype(np.float32)
+    if beta is None:
+        beta = sigmoid(rng.standard_normal((T, H))).astype(np.float32)
+    else:
+        beta = np.full((T, H), beta, np.float32)
+    if g is None:
+        if decay == "sigmoid":
+            g = (-5.0 * sigmoid(rng.standard_normal((T, H, d)) - 4.0)).astype(np.float32)
+        else:
+            g = (-5.0 * (1.0 - rng.random((T, H, d)))).astype(np.float32)
+    else:
+        g = np.full((T, H, d), g, np.float32)
+    S0 = None if s0_std is None else (rng.standard_normal((1, H, d, d)) * s0_std).astype(np.float32)
+    return dict(q=q, k=k, v=v, g=g, beta=beta, S0=S0)
+
+
+def run(c, cu=None, every=False, **kw):
+    T = c["q"].shape[0]
+    cu = np.array([0, T], np.int32) if cu is None else np.asarray(cu, np.int32)
+    off = pos = None
+    if every:  # a checkpoint after every token: exposes S_t for all t
+        lens = np.diff(cu)
+        off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        pos = np.concatenate([np.arange(1, n + 1) for n in lens]).astype(np.int32)
+    return oracle.prefill(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, S_in=c["S0"],
+                          ckpt_off=off, ckpt_pos=pos, **kw)
+
+
+def exact_unit_keys(n, d, seed):
+    """Keys with entries +-1/4 on 16 channels: unit norm exactly in binary floating point."""
+    rng = np.random.default_rng(seed)
+    k = np.zeros((n, d), np.float32)
+    for i in range(n):
+        ch = rng.choice(d, 16, replace=False)
+        k[i, ch] = rng.choice([-0.25, 0.25], 16)
+    return k
+
+
+def hadamard16():
+    h = np.array([[1.0]])
+    for _ in range(4):
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+# ---------------------------------------------------------------- closed forms [p1 3.1]
+def pin_single_token():
+    """From S = 0 one token gives S_1 = beta k v^T and o_1 = beta (q . k) v."""
+    c = rand_case(1, 3, 32, seed=11, s0_std=None)
+    r = run(c)
+    for h in range(3):
+        q, k, v = (c[x][0, h].astype(np.float64) for x in ("q", "k", "v"))
+        b = float(c["beta"][0, h])
+        np.testing.assert_allclose(r["S_out"][0, h], b * np.outer(k, v), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(r["o"][0, h], b * np.dot(q, k) * v, rtol=0, atol=1e-14)
+
+
+def pin_decay_only():
+    """beta = 0: S_t = Diag(exp(sum_{r<=t} g_r)) S_0 (natural exp), o_t = S_t^T q_t."""
+    c = rand_case(40, 2, 24, seed=12, decay="uniform", beta=0.0)
+    r = run(c, every=True)
+    G = np.cumsum(c["g"].astype(np.float64), axis=0)
+    for h in range(2):
+        S0 = c["S0"][0, h].astype(np.float64)
+        for t in (0, 7, 39):
+            St = np.exp(G[t, h])[:, None] * S0
+            np.testing.assert_allclose(r["ckpts"][t, h], St, rtol=1e-12, atol=1e-300)
+            np.testing.assert_allclose(r["o"][t, h], St.T @ c["q"][t, h].astype(np.float64),
+                                       rtol=1e-11, atol=1e-300)
+
+
+def pin_identity_token():
+    """beta = 0 and g = 0 leave the state bit-for-bit unchanged and o_t = S_0^T q_t."""
+    c = rand_case(17, 2, 16, seed=13, beta=0.0, g=0.0)
+    r = run(c)
+    assert np.array_equal(r["S_out"][0], c["S0"][0].astype(np.float64))
+    for h in range(2):
+        np.testing.assert_allclose(r["o"][:, h], c["q"][:, h].astype(np.float64) @ c["S0"][0, h].astype(np.float64),
+                                   rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------ delta rule [p2 4, p1 3.1]
+def pin_retrieval():
+    """beta = 1, |k| = 1: S_t^T k_t = v_t after every token, whatever the decay and S_0
+    (the update overwrites the value stored under the current key; decay acts first)."""
+    T, H, d = 30, 2, 64
+    c = rand_case(T, H, d, seed=14, decay="uniform", beta=1.0)
+    for h in range(H):
+        c["k"][:, h] = exact_unit_keys(T, d, seed=100 + h)
+    r = run(c, every=True)
+    for t in range(T):
+        for h in range(H):
+            got = r["ckpts"][t, h].T @ c["k"][t, h].astype(np.float64)
+            np.testing.assert_allclose(got, c["v"][t, h], rtol=0, atol=1e-12)
+
+
+def pin_orthonormal_write():
+    """alpha = 1, beta = 1, S_0 = 0, d orthonormal keys: afterwards S^T k_i = v_i for all i."""
+    d = 64
+    K = np.zeros((d, d))
+    for b in range(d // 16):
+        K[16 * b:16 * b + 16, 16 * b:16 * b + 16] = hadamard16() / 4.0
+    perm = np.random.default_rng(15).permutation(d)
+    K = K[perm]
+    c = rand_case(d, 1, d, seed=15, beta=1.0, g=0.0, s0_std=None)
+    c["k"][:, 0] = K.astype(np.float32)
+    r = run(c)
+    S = r["S_out"][0, 0]
+    np.testing.assert_allclose(K @ S, c["v"][:, 0], rtol=0, atol=1e-13)
+
+
+def pin_matrix_form():
+    """Brute force on tiny d: S_t = (I - beta k k^T) Diag(exp g) S_{t-1} + beta k v^T with
+    explicit d x d matrices, o_t = S_t^T q_t."""
+    for d, seed in ((4, 16), (7, 17)):
+        c = rand_case(12, 2, d, seed=seed, decay="uniform")
+        r = run(c, every=True)
+        for h in range(2):
+            S = c["S0"][0, h].astype(np.float64)
+            for t in range(12):
+                k = c["k"][t, h].astype(np.float64)
+                b = float(c["beta"][t, h])
+                A = np.eye(d) - b * np.outer(k, k)
+                S = A @ np.diag(np.exp(c["g"][t, h].astype(np.float64))) @ S + b * np.outer(k, c["v"][t, h])
+                np.testing.assert_allclose(r["ckpts"][t, h], S, rtol=1e-12, atol=1e-14)
+                np.testing.assert_allclose(r["o"][t, h], S.T @ c["q"][t, h], rtol=1e-12, atol=1e-14)
+
+
+def pin_linearity():
+    """For fixed q, k, g, beta the result is linear in (S_0, V) jointly."""
+    c = rand_case(50, 2, 32, seed=18, decay="uniform")
+    full = run(c)
+    c_s = dict(c, v=np.zeros_like(c["v"]))
+    c_v = dict(c, S0=None)
+    a, b = run(c_s), run(c_v)
+    np.testing.assert_allclose(full["S_out"], a["S_out"] + b["S_out"], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(full["o"], a["o"] + b["o"], rtol=1e-11, atol=1e-13)
+
+
+# ------------------------------------------------------- chunk form [p2 6] and [p1 3.2]
+def pin_chunk_form(Cs=(1, 2, 4, 16, 64), Ts=(1, 5, 63, 64, 65, 130, 300)):
+    """The chunk-level matrix form equals the per-token oracle (partial last chunks
+    included), for both the typical and the stress decay distribution."""
+    for decay, seed in (("sigmoid", 19), ("uniform", 20)):
+        c = rand_case(max(Ts), 1, 32, seed=seed, decay=decay)
+        for T in Ts:
+            cc = {k: (v[:T] if k != "S0" else v) for k, v in c.items()}
+            ref = run(cc)
+            for C in Cs:
+                O, S = chunked.prefill_one(cc["q"][:, 0], cc["k"][:, 0], cc["v"][:, 0], cc["g"][:, 0],
+                                           cc["beta"][:, 0], cc["S0"][0, 0], C)
+                scale = np.abs(ref["o"]).max()
+                np.testing.assert_allclose(O, ref["o"][:, 0], rtol=0, atol=1e-9 * scale)
+                np.testing.assert_allclose(S, ref["S_out"][0, 0], rtol=0, atol=1e-9 * np.abs(S).max())
+
+
+# ------------------------------------------------------------- segment algebra [p3 2]
+def pin_segments():
+    """Exit state = S~ + M S_in for a split anywhere; the combine is associative; M is the
+    state reached from S_in = I with V = 0."""
+    T, d = 90, 16
+    c = rand_case(T, 1, d, seed=21, decay="uniform")
+    ref = run(c)
+    S_in = c["S0"][0, 0].astype(np.float64)
+
+    def pair(a, b):
+        sub = {k: (v[a:b] if k != "S0" else None) for k, v in c.items()}
+        St = run(sub)["S_out"][0, 0]
+        return segments.transition(c["k"][a:b, 0], c["g"][a:b, 0], c["beta"][a:b, 0]), St
+
+    for cuts in ((0, 37, T), (0, 1, 50, T), (0, 30, 60, T)):
+        pairs = [pair(a, b) for a, b in zip(cuts[:-1], cuts[1:])]
+        _, S_exit = segments.entry_states(pairs, S_in)
+        np.testing.assert_allclose(S_exit, ref["S_out"][0, 0], rtol=0, atol=1e-11)
+    p1, p2, p3 = pair(0, 20), pair(20, 55), pair(55, T)
+    L = segments.combine(segments.combine(p1, p2), p3)
+    R = segments.combine(p1, segments.combine(p2, p3))
+    np.testing.assert_allclose(L[0], R[0], atol=1e-12)
+    np.testing.assert_allclose(L[1], R[1], atol=1e-12)
+    cI = dict(c, v=np.zeros_like(c["v"]), S0=np.eye(d, dtype=np.float32)[None, None])
+    np.testing.assert_allclose(run(cI)["S_out"][0, 0],
+                               segments.transition(c["k"][:, 0], c["g"][:, 0], c["beta"][:, 0]),
+                               rtol=0, atol=1e-12)
+
+
+# ------------------------------------------- packing, checkpoints, restart [p3 3.2-3.3]
+def pin_restart_2560():
+    """A request matched up to 2800 tokens resumes at 2560 = 5 x 512: resuming from the
+    checkpoint at 2560 with the remaining tokens reproduces the continuous run."""
+    T, H, d, P = 2800, 2, 16, 2560
+    c = rand_case(T, H, d, seed=22)
+    off = np.array([0, T // 512], np.int32)
+    pos = np.arange(512, T + 1, 512, dtype=np.int32)
+    full = oracle.prefill(c["q"], c["k"], c["v"], c["g"], c["beta"], np.array([0, T], np.int32),
+                          S_in=c["S0"], ckpt_off=off, ckpt_pos=pos)
+    assert list(pos) == [512, 1024, 1536, 2048, 2560]
+    ck = full["ckpts"][list(pos).index(P)]
+    tail = {k: (v[P:] if k != "S0" else ck[None].astype(np.float32)) for k, v in c.items()}
+    rest = run(tail)
+    np.testing.assert_allclose(rest["S_out"][0], full["S_out"][0], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(rest["o"], full["o"][P:], rtol=0, atol=1e-6)
+
+
+def pin_packing_and_checkpoints():
+    """Packed sequences equal separate runs bit for bit; the checkpoint at p = len is
+    S_out; the checkpoint at p equals the final state of the run truncated to p tokens;
+    unit and row subsets reproduce the full run."""
+    lens = [5, 64, 1, 100, 33]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, H, d = int(cu[-1]), 3, 16
+    c = rand_case(T, H, d, seed=23, decay="uniform")
+    rng = np.random.default_rng(23)
+    c["S0"] = (rng.standard_normal((len(lens), H, d, d)) * 0.1).astype(np.float32)
+    pos, off = [], [0]
+    for n in lens:
+        p = sorted(set(rng.choice(np.arange(1, n + 1), size=min(3, n), replace=False).tolist()) | {n})
+        pos += p
+        off.append(len(pos))
+    off, pos = np.array(off, np.int32), np.array(pos, np.int32)
+    full = oracle.prefill(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, S_in=c["S0"],
+                          ckpt_off=off, ckpt_pos=pos)
+    for i, n in enumerate(lens):
+        a, b = cu[i], cu[i + 1]
+        sub = {k: (v[a:b] if k != "S0" else v[i:i + 1]) for k, v in c.items()}
+        one = run(sub)
+        assert np.array_equal(one["o"], full["o"][a:b])
+        assert np.array_equal(one["S_out"][0], full["S_out"][i])
+        for j in range(off[i], off[i + 1]):
+            p = int(pos[j])
+            trunc = run({k: (v[:p] if k != "S0" else v) for k, v in sub.items()})
+            assert np.array_equal(trunc["S_out"][0], full["ckpts"][j])
+        assert np.array_equal(full["ckpts"][off[i + 1] - 1], full["S_out"][i])
+    units = np.array([1, 5, 14], np.int64)
+    rows = np.array([0, 3, 70, T - 1], np.int64)
+    part = oracle.prefill(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, S_in=c["S0"],
+                          units=units, o_rows=rows)
+    for u in units:
+        s, h = divmod(int(u), H)
+        assert np.array_equal(part["S_out"][s, h], full["S_out"][s, h])
+        for ri, r in enumerate(rows):
+            if cu[s] <= r < cu[s + 1]:
+                assert np.array_equal(part["o"][ri, h], full["o"][r, h])
+
+
+def pin_decode_commit():
+    """Verify step [p1 3.4, p3 4]: outputs of all n_tok tokens, state after n_commit."""
+    B, n, H, d = 5, 4, 2, 16
+    c = rand_case(B * n, H, d, seed=24)
+    rng = np.random.default_rng(24)
+    S0 = (rng.standard_normal((B, H, d, d)) * 0.02).astype(np.float32)
+    n_commit = np.array([0, 1, 2, 3, 4], np.int32)
+    shp = lambda x: x.reshape((B, n) + x.shape[1:])
+    r = oracle.decode(shp(c["q"]), shp(c["k"]), shp(c["v"]), shp(c["g"]), shp(c["beta"]), S0, n_commit)
+    for b in range(B):
+        sub = {k: v[b * n:(b + 1) * n] for k, v in c.items() if k != "S0"}
+        sub["S0"] = S0[b:b + 1]
+        ref = run(sub, every=True)
+        assert np.array_equal(r["o"][b], ref["o"])
+        want = S0[b].astype(np.float64) if n_commit[b] == 0 else ref["ckpts"][n_commit[b] - 1]
+        assert np.array_equal(r["S"][b], want)
+
+
+ALL_PINS = [pin_single_token, pin_decay_only, pin_identity_token, pin_retrieval,
+            pin_orthonormal_write, pin_matrix_form, pin_linearity, pin_chunk_form,
+            pin_segments, pin_restart_2560, pin_packing_and_checkpoints, pin_decode_commit]

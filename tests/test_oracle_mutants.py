@@ -1,0 +1,54 @@
+"""Plausible mistakes planted in a copy of the oracle (on the CPU) must each fail a pin.
+
+Each mutant is the oracle's C source with one textual change, compiled into a temporary
+library and swapped in for the real one while the pins run."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "decay_scales_columns": ("Si[j] *= al[i];", "Si[j] *= al[j];"),
+    "beta_dropped": ("u[j] = beta * (v[j] - u[j]);", "u[j] = (v[j] - u[j]);"),
+    "delta_sign_flipped": ("u[j] = beta * (v[j] - u[j]);", "u[j] = beta * (v[j] + u[j]);"),
+    "readout_transposed": ("u[j] += Si[j] * k[i];", "u[j] += S[(int64_t)j * d + i] * k[i];"),
+    "outer_product_transposed": ("Si[j] += k[i] * u[j];", "Si[j] += k[j] * u[i];"),
+    "output_reads_key": ("o[j] += Si[j] * q[i];", "o[j] += Si[j] * k[i];"),
+    "decay_base_two": ("al[i] = exp((double)a->g[base + i]);", "al[i] = exp2((double)a->g[base + i]);"),
+    "checkpoint_off_by_one": ("a->ckpt_pos[c] == t + 1", "a->ckpt_pos[c] == t + 2"),
+    "initial_state_ignored": ("S[e] = (double)s0[e];", "S[e] = 0.0 * (double)s0[e];"),
+}
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "kda_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / f"lib{name}.so"
+    inc = os.path.dirname(oracle.__file__)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", f"-I{inc}",
+                    "-o", str(so), str(path), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    lib.kda_ref_run.restype = ctypes.c_int
+    lib.kda_ref_run.argtypes = [ctypes.POINTER(oracle._Args), ctypes.POINTER(ctypes.c_int)]
+    return lib
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name, monkeypatch):
+    old, new = MUTANTS[name]
+    lib = _build_mutant(tmp_path, name, old, new)
+    oracle._load()
+    monkeypatch.setattr(oracle, "_lib", lib)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, oracle.OracleError):
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
