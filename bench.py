@@ -1,0 +1,350 @@
+#!/usr/bin/env python3
+"""Benchmark: KDA prefill tokens/s at model width (1 x 8192 tokens, 96 heads of 128) and
+decode state GB/s (256 sequences x 96 heads), each against the GB300 roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one kda_prefill call over the whole 8192 x 96 workload (inputs resident in
+HBM, 1.2 GB > L2, so no flush is needed).  Decode is timed the same way on its own and
+reported in the "decode" object.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
+same workload (the oracle is the only reference implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=96,d=128) + decode state GB/s, as % of GB300 roofline"
+WORKLOAD = "prefill_8k"
+D, C = 128, 64
+# Algorithmic work per (token, head) at C = 64 ("Kimi K3 ... 服務性能" section 6: 12C^3 +
+# 8C^2 D + 6CD^2 FLOPs per chunk) and the minimum bytes: q, k, v bf16 (768) + g fp32
+# (512) + beta (4) + o bf16 (256).
+PREFILL_FLOP_PER_TOKEN_HEAD = (12 * C**3 + 8 * C**2 * D + 6 * C * D**2) / C
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 2 * D + 4 * D + 4 + 2 * D
+STATE_BYTES = D * D * 4
+# Decode per (sequence, head, token): the pages' 8 D^2 bytes of fp32 state (read + write)
+# and 7 D^2 FLOPs; per-token inputs/outputs: q, k, v bf16, g fp32, beta, o fp32.
+DECODE_STATE_BYTES = 8 * D * D
+DECODE_IO_BYTES = 3 * 2 * D + 4 * D + 4 + 4 * D
+DECODE_FLOP = 7 * D * D
+CPU_SAMPLE_TOKENS = 2048
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mhz = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------ CPU oracle
+def oracle_sample(x, n_tokens, threads=0):
+    """The oracle on the first n_tokens of every head of the workload; returns (seconds,
+    threads used, token-heads)."""
+    import numpy as np
+    import torch
+    import oracle
+    oracle.build()
+    sl = lambda t: t[:n_tokens].contiguous().cpu()
+    bits = lambda t: sl(t).view(torch.int16).numpy().view(np.uint16)
+    q, k, v = bits(x.q), bits(x.k), bits(x.v)
+    g, beta = sl(x.g).numpy(), sl(x.beta).numpy()
+    cu = np.array([0, n_tokens], np.int32)
+    t0 = time.perf_counter()
+    r = oracle.prefill(q, k, v, g, beta, cu, want_o=True, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, r["threads"], n_tokens * x.q.shape[1]
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: K timed steps of the bounded sample on rank 0."""
+    if rank != 0:
+        return
+    import torch
+    from kimi_delta_attention_prefill_gb300 import inputs
+    x = inputs.make_workload(WORKLOAD, device="cpu")
+    n = CPU_SAMPLE_TOKENS
+    for _ in range(args.warmup):
+        oracle_sample(x, n)
+    times, threads = [], 0
+    for _ in range(args.steps):
+        dt, threads, _ = oracle_sample(x, n)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = n / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B=1, H=96, T=8192, d=128 (oracle sample: first {n} tokens of every head)",
+                   "global_batch": 1, "seq_len": 8192},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {n} of 8192 tokens, all 96 heads, fp64 per-token recurrence"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- ours
+def run_ours(args, world, rank, local):
+    import torch
+    import kimi_delta_attention_prefill_gb300 as kda
+    from kimi_delta_attention_prefill_gb300 import inputs
+
+    peaks = load_peaks()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    x = inputs.make_workload(WORKLOAD, device=dev)
+    T, H = x.q.shape[0], x.q.shape[1]
+    cu = x.cu_seqlens.to(dev)
+    o = torch.empty_like(x.q)
+    S = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    ws_n = kda.prefill_workspace_size(1, H, T)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+    launches_per_prefill = 1  # one kernel per call (no segment split chosen at 96 heads)
+
+    def step():
+        kda.prefill(x.q, x.k, x.v, x.g, x.beta, cu, o=o, S_out=S, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    value = world * T / (ms / 1e3)
+
+    # roofline of the (single) prefill kernel: algorithmic bytes / launch duration
+    alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    alg_flop = T * H * PREFILL_FLOP_PER_TOKEN_HEAD
+    launch_s = ms_local / 1e3 / launches_per_prefill
+    achieved_gbs = alg_bytes / launch_s / 1e9
+    achieved_tflops = alg_flop / launch_s / 1e12
+
+    # decode: 256 sequences x 96 heads, one token; state stream against HBM
+    dx = inputs.make_workload("decode", device=dev)
+    Sd = dx.S0.clone()
+    od = torch.empty((256, 1, H, D), dtype=torch.float32, device=dev)
+
+    def dstep():
+        kda.decode(dx.q, dx.k, dx.v, dx.g, dx.beta, Sd, o=od, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        dstep()
+    torch.cuda.synchronize(dev)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dsteps = max(args.steps, 20)
+    d0.record(stream)
+    for _ in range(dsteps):
+        dstep()
+    d1.record(stream)
+    torch.cuda.synchronize(dev)
+    dms = d0.elapsed_time(d1) / dsteps
+    n_units = 256 * H
+    dec_bytes = n_units * (DECODE_STATE_BYTES + DECODE_IO_BYTES)
+    dec_gbs = n_units * DECODE_STATE_BYTES / (dms / 1e-3) / 1e9 if False else n_units * DECODE_STATE_BYTES / (dms / 1e3) / 1e9
+    dec_all_gbs = dec_bytes / (dms / 1e3) / 1e9
+
+    # end to end through the public call, host buffers: pinned H2D of the step's inputs,
+    # the prefill, D2H of o and the final state
+    hq, hk, hv, hg, hb = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta))
+    hcu = x.cu_seqlens.pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hS = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    dq, dk, dv, dg, db = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    dcu = torch.empty_like(cu)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hcu))
+    d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
+
+    def e2e_step():
+        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb), (dcu, hcu)):
+            dst.copy_(src, non_blocking=True)
+        kda.prefill(dq, dk, dv, dg, db, dcu, o=o, S_out=S, workspace=ws, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hS.copy_(S, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
+    e2e_value = world * T / (e_ms / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, threads, th = oracle_sample(x, CPU_SAMPLE_TOKENS)
+        cpu = {"value": CPU_SAMPLE_TOKENS / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {CPU_SAMPLE_TOKENS} of 8192 tokens, all 96 heads ({th} token-heads), "
+                         f"fp64 per-token recurrence, {dt:.2f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: B=1, H=96, T=8192, d=128, C=64, zero initial state, "
+                                   "q/k L2-normalised bf16, v bf16, g/beta fp32",
+                       "global_batch": world, "seq_len": T, "heads": H, "head_dim": D,
+                       "l2": "inputs (1.2 GB) larger than L2 (129 MB); no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "prefill_kernel", "bytes_per_launch": alg_bytes,
+                         "peak_source": peaks["source"],
+                         "tensor": {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                    "frac": achieved_tflops / peaks["bf16_tflops"],
+                                    "flop_per_launch": alg_flop}},
+            "decode": {"metric": "KDA decode state GB/s (256 x 96 heads, 1 token)", "value": dec_gbs,
+                       "unit": "GB/s", "us_per_step": dms * 1e3,
+                       "roofline": {"bound": "hbm", "achieved": dec_all_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": dec_all_gbs / peaks["hbm_gbs"], "traffic": None,
+                                    "kernel": "decode_kernel", "bytes_per_launch": dec_bytes}},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_prefill * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        from kimi_delta_attention_prefill_gb300 import build as kbuild
+        if rank == 0 and not kbuild.up_to_date():
+            kbuild.build()
+        barrier(world)
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

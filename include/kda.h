@@ -1,0 +1,135 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * The operation (per head; "Kimi K3.1 Pro 架构完全拆解", section 3.1):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t,          alpha_t = exp(g_t) per d_k channel
+ *
+ * with S_t a d_k x d_v matrix (row = d_k channel, column = d_v channel) and g the
+ * natural-log decay, bounded below by g_min = -5 (section 3.2 of the same page).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - d_k = d_v = d = 128 (KDA_HEAD_DIM); any other d returns KDA_ERR_UNSUPPORTED.
+ *  - Every pointer argument is a DEVICE pointer on the current CUDA device, owned by
+ *    the caller.  The library allocates no device memory and keeps no state between
+ *    calls.  Tensor pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT otherwise).
+ *  - Calls are asynchronous on `stream`: they validate what the host can see, enqueue
+ *    kernels and return.  A non-KDA_OK return means nothing was enqueued (except
+ *    KDA_ERR_CUDA, returned when a launch itself failed).
+ *  - `dev_status` (optional, device int): kernels that find a problem only visible on
+ *    the device (inconsistent cu_seqlens / checkpoint contents, an n_commit out of
+ *    range, a bounded wait that ran out) write a kda_status code there, first error
+ *    wins; the work unit concerned is skipped.  The library never clears it: zero it
+ *    before the call and read it after synchronising.  NULL disables the report.
+ *  - Element types: kda_bf16 is the IEEE bfloat16 bit pattern; float is IEEE fp32.
+ *  - Input ranges the tensor-core path relies on: q and k L2-normalised per (token,
+ *    head) (the model normalises them before the recurrence), |v| well below 6e4, and
+ *    g in [-5, 0].  Outside them results may overflow to inf/NaN.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kda_bf16;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent sizes */
+  KDA_ERR_UNSUPPORTED = 2,   /* d != 128, n_tok outside [1, 4], no sm_103a device */
+  KDA_ERR_ALIGNMENT = 3,     /* a tensor pointer not 16-byte aligned */
+  KDA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+  KDA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+  KDA_ERR_TIMEOUT = 6,       /* device-side: a bounded wait ran out (written to dev_status) */
+  KDA_ERR_DEVICE_CHECK = 7   /* device-side: argument contents inconsistent (dev_status) */
+} kda_status;
+
+#define KDA_HEAD_DIM 128
+#define KDA_CHUNK 64
+#define KDA_MAX_DECODE_TOKENS 4
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kda_status_string(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+int kda_version(void);
+
+/*
+ * kda_decode -- one decode step, or a verify step of up to 4 tokens, per (sequence, head).
+ *
+ * Source: "Kimi K3 ... 服務性能" (SemiAnalysis translation) section 6: the decode kernel
+ * follows the delta-rule form
+ *     X = Diag(alpha_t) S;  u_t = beta_t (v_t - X^T k_t);  S = X + k_t u_t^T;  o_t = S^T q_t.
+ * Verify ("Kimi K3.1 Pro 架构完全拆解" 3.4; "部署 Kimi K3 ..." section 4): the n_tok
+ * cached projected inputs are replayed on-chip and only the state after the accepted
+ * prefix is written back.
+ *
+ *   q, k, v    [B, n_tok, H, d]  bf16       g  [B, n_tok, H, d] fp32    beta [B, n_tok, H] fp32
+ *   S_state    [B, H, d, d]      fp32, read, then overwritten in place with the state
+ *                                after n_commit[b] tokens (left untouched when 0)
+ *   n_commit   [B] int32 in [0, n_tok], or NULL for n_tok; an entry out of range leaves
+ *              that sequence's state untouched and reports KDA_ERR_DEVICE_CHECK
+ *   o          [B, n_tok, H, d]  fp32: outputs of all n_tok tokens
+ *   1 <= n_tok <= 4.  B or H == 0 is a no-op.
+ */
+kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
+                      float* S_state, const int32_t* n_commit, float* o, int B, int n_tok, int H, int d,
+                      int* dev_status, cudaStream_t stream);
+
+/*
+ * kda_prefill_workspace_size -- bytes of device workspace kda_prefill needs for the
+ * same (n_seq, H, d, total_tokens, n_segments).  0 means no workspace is needed.
+ */
+size_t kda_prefill_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int n_segments);
+
+/*
+ * kda_prefill -- chunkwise prefill over packed variable-length sequences.
+ *
+ * Sources: the chunk-level matrix form of "Kimi K3 ... 服務性能" section 6 (FlashKDA
+ * algorithm: prep a = exp(cumsum g), K_decay, Q_decay, K_inv, K_restore, L, INV, M_qk;
+ * recurrence U = INV Diag(beta)(V - K_decay S), O = Q_decay S + M_qk U,
+ * S <- Diag(a_last) S + K_restore^T U) with chunk length C = 64; the sequence split of
+ * "部署 Kimi K3 ..." sections 1.2 and 2 (per-segment transition M and zero-start
+ * state S~, entry states by an associative prefix scan S = S~ + M S_in); state
+ * checkpoints at requested positions (same page, section 3.2).
+ *
+ *   q, k, v      [total_tokens, H, d]  bf16
+ *   g            [total_tokens, H, d]  fp32      beta [total_tokens, H] fp32
+ *   S_in         [n_seq, H, d, d] fp32 initial states (read only), or NULL for zeros
+ *   cu_seqlens   [n_seq + 1] int32: sequence i owns packed rows [cu[i], cu[i+1]);
+ *                cu[0] = 0, non-decreasing, cu[n_seq] = total_tokens (checked on device)
+ *   ckpt_off     [n_seq + 1] int32 CSR offsets into ckpt_pos (or NULL: no checkpoints)
+ *   ckpt_pos     [n_ckpt] int32: for sequence i, positions ckpt_pos[ckpt_off[i] ..
+ *                ckpt_off[i+1]) strictly increasing in (0, len_i], each a multiple of
+ *                64 or equal to len_i.  A position p means "the state after the
+ *                sequence's p-th token of this call".  Violations: KDA_ERR_DEVICE_CHECK.
+ *   o            [total_tokens, H, d] bf16 (round to nearest even from fp32)
+ *   S_out        [n_seq, H, d, d] fp32 final states, or NULL
+ *   ckpts        [n_ckpt, H, d, d] fp32, slot j = checkpoint ckpt_pos[j] (write only)
+ *   n_segments   0: the library splits long sequences by its own rule (a function of the
+ *                sequence's own length, H and the SM count only, so a sequence gives the
+ *                same bits packed or alone); k >= 1: split every sequence into
+ *                min(k, its chunk count) segments.
+ *   workspace    device buffer of kda_prefill_workspace_size(...) bytes (may be NULL
+ *                when that is 0), 256-byte aligned.
+ * Output rows of other sequences, and padding, are never written.
+ */
+kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
+                       const float* S_in, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                       const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* o,
+                       float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
+                       size_t workspace_bytes, int* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,1 +1,179 @@
-"""GB300-native Kimi Delta Attention (KDA) prefill / decode."""
+"""GB300-native Kimi Delta Attention (KDA): chunkwise prefill and decode / verify.
+
+Python binding of the C ABI in ``include/kda.h``: argument marshalling only.  Every
+step of the computation runs in the CUDA kernels of ``libkda.so`` (sm_103a); there is
+no CPU or PyTorch fallback, and a missing library raises ``KdaLibraryError``.
+
+Functions mirror the C entry points: :func:`prefill` (``kda_prefill``),
+:func:`decode` (``kda_decode``), :func:`prefill_workspace_size`
+(``kda_prefill_workspace_size``), :func:`status_string` (``kda_status_string``).
+Tensors are torch CUDA tensors; the launch goes to the current torch stream unless
+``stream`` is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+HEAD_DIM = 128
+CHUNK = 64
+MAX_DECODE_TOKENS = 4
+
+_lib = None
+_lock = threading.Lock()
+
+_c_int, _c_i64, _c_sz, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+
+
+class KdaLibraryError(RuntimeError):
+    """The compiled CUDA library is missing or cannot be loaded."""
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def library():
+    """Load ``libkda.so`` (built by ``kimi_delta_attention_prefill_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise KdaLibraryError(
+                    f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+            try:
+                lib = ctypes.CDLL(LIB_PATH)
+            except OSError as e:  # pragma: no cover - depends on the host
+                raise KdaLibraryError(f"cannot load {LIB_PATH}: {e}") from e
+            lib.kda_status_string.restype = ctypes.c_char_p
+            lib.kda_status_string.argtypes = [_c_int]
+            lib.kda_version.restype = _c_int
+            lib.kda_version.argtypes = []
+            lib.kda_decode.restype = _c_int
+            lib.kda_decode.argtypes = [_vp] * 8 + [_c_int] * 4 + [_vp, _vp]
+            lib.kda_prefill_workspace_size.restype = _c_sz
+            lib.kda_prefill_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_i64, _c_int]
+            lib.kda_prefill.restype = _c_int
+            lib.kda_prefill.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
+                                        [_c_int, _c_int, _c_int, _vp, _c_sz, _vp, _vp])
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().kda_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return library().kda_version()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def decode(q, k, v, g, beta, S_state, n_commit=None, o=None, dev_status=None, stream=None):
+    """One decode (n_tok = 1) or verify (n_tok <= 4) step; updates ``S_state`` in place.
+
+    q, k, v ``[B, n_tok, H, 128]`` bf16; g ``[B, n_tok, H, 128]`` fp32; beta
+    ``[B, n_tok, H]`` fp32; S_state ``[B, H, 128, 128]`` fp32; n_commit ``[B]`` int32 or
+    None.  Returns o ``[B, n_tok, H, 128]`` fp32.
+    """
+    B, n_tok, H, d = q.shape
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape)
+    _need(beta, "beta", torch.float32, (B, n_tok, H))
+    _need(S_state, "S_state", torch.float32, (B, H, d, d))
+    if n_commit is not None:
+        _need(n_commit, "n_commit", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, n_tok, H, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, n_tok, H, d))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_state), _ptr(n_commit),
+                              _ptr(o), B, n_tok, H, d, _ptr(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_decode")
+    return o
+
+
+def prefill_workspace_size(n_seq, H, total_tokens, n_segments=0, d=HEAD_DIM) -> int:
+    return int(library().kda_prefill_workspace_size(int(n_seq), int(H), int(d), int(total_tokens),
+                                                    int(n_segments)))
+
+
+def prefill(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt_pos=None, o=None, S_out=None,
+            ckpts=None, n_segments=0, workspace=None, dev_status=None, stream=None):
+    """Chunkwise prefill over packed sequences.
+
+    q, k, v ``[T, H, 128]`` bf16; g ``[T, H, 128]`` fp32; beta ``[T, H]`` fp32;
+    cu_seqlens ``[N+1]`` int32 (device); S_in ``[N, H, 128, 128]`` fp32 or None;
+    ckpt_off ``[N+1]`` / ckpt_pos ``[n_ckpt]`` int32 (device) or None.
+    Returns ``(o, S_out, ckpts)``.
+    """
+    T, H, d = q.shape
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape)
+    _need(beta, "beta", torch.float32, (T, H))
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seq = cu_seqlens.shape[0] - 1
+    if S_in is not None:
+        _need(S_in, "S_in", torch.float32, (n_seq, H, d, d))
+    n_ckpt = 0
+    if ckpt_off is not None:
+        _need(ckpt_off, "ckpt_off", torch.int32, (n_seq + 1,))
+        _need(ckpt_pos, "ckpt_pos", torch.int32)
+        n_ckpt = ckpt_pos.shape[0]
+        if ckpts is None:
+            ckpts = torch.empty((n_ckpt, H, d, d), dtype=torch.float32, device=q.device)
+        _need(ckpts, "ckpts", torch.float32, (n_ckpt, H, d, d))
+    if o is None:
+        o = torch.empty((T, H, d), dtype=torch.bfloat16, device=q.device)
+    _need(o, "o", torch.bfloat16, (T, H, d))
+    if S_out is None:
+        S_out = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=q.device)
+    _need(S_out, "S_out", torch.float32, (n_seq, H, d, d))
+    ws_need = prefill_workspace_size(n_seq, H, T, n_segments, d)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_in), _ptr(cu_seqlens),
+                               n_seq, T, _ptr(ckpt_off), _ptr(ckpt_pos), n_ckpt, _ptr(o), _ptr(S_out),
+                               _ptr(ckpts), H, d, int(n_segments), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                               _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_prefill")
+    return o, S_out, ckpts

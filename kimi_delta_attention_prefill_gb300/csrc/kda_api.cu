@@ -1,0 +1,121 @@
+// kda_api.cu -- the C ABI (include/kda.h): host-side validation and launch.
+//
+// Nothing here allocates device memory or keeps per-call state; the only cached
+// values are per-device properties (compute capability, SM count).
+#include <cuda_runtime.h>
+#include <atomic>
+#include <cstdint>
+
+#include "kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_cc[kMaxDevices];   // 0 = unknown, else major*10+minor
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+// Returns KDA_OK when the current device is an sm_103 part; fills its SM count.
+kda_status current_device(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KDA_ERR_CUDA;
+  int cc = dev < kMaxDevices ? g_dev_cc[dev].load(std::memory_order_relaxed) : 0;
+  int n = dev < kMaxDevices ? g_dev_sms[dev].load(std::memory_order_relaxed) : 0;
+  if (cc == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    cc = major * 10 + minor;
+    if (dev < kMaxDevices) {
+      g_dev_sms[dev].store(n, std::memory_order_relaxed);
+      g_dev_cc[dev].store(cc, std::memory_order_relaxed);
+    }
+  }
+  if (sms) *sms = n;
+  return cc == 103 ? KDA_OK : KDA_ERR_UNSUPPORTED;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_ALIGNMENT: return "KDA_ERR_ALIGNMENT";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK";
+    default: return "KDA_ERR_UNKNOWN";
+  }
+}
+
+int kda_version(void) { return 100; }
+
+kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
+                      float* S_state, const int32_t* n_commit, float* o, int B, int n_tok, int H, int d,
+                      int* dev_status, cudaStream_t stream) {
+  if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (n_tok < 1 || n_tok > KDA_MAX_DECODE_TOKENS) return KDA_ERR_UNSUPPORTED;
+  if (B < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return KDA_OK;
+  if (!q || !k || !v || !g || !beta || !S_state || !o) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(S_state, 16) ||
+      !aligned(o, 16) || !aligned(beta, 4) || !aligned(n_commit, 4) || !aligned(dev_status, 4))
+    return KDA_ERR_ALIGNMENT;
+  kda_status st = current_device(nullptr);
+  if (st != KDA_OK) return st;
+  cudaError_t e = kda::launch_decode(q, k, v, g, beta, S_state, n_commit, o, B, n_tok, H, dev_status, stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t kda_prefill_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int n_segments) {
+  if (d != KDA_HEAD_DIM || n_seq < 0 || H <= 0 || total_tokens < 0 || n_segments < 0) return 0;
+  int sms = 0;
+  if (current_device(&sms) != KDA_OK) sms = 152;
+  return kda::prefill_workspace_bytes(n_seq, H, total_tokens, n_segments, sms);
+}
+
+kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
+                       const float* S_in, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                       const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* o,
+                       float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
+                       size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (n_seq < 0 || H < 0 || total_tokens < 0 || n_ckpt < 0 || n_segments < 0) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0x7fffffffLL || static_cast<int64_t>(n_seq) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (n_seq == 0 || H == 0) return KDA_OK;
+  if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+  if (ckpt_off == nullptr && n_ckpt != 0) return KDA_ERR_INVALID_ARG;
+  if (ckpt_off != nullptr && n_ckpt > 0 && (!ckpt_pos || !ckpts)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(o, 16) ||
+      !aligned(S_in, 16) || !aligned(S_out, 16) || !aligned(ckpts, 16) || !aligned(beta, 4) ||
+      !aligned(cu_seqlens, 4) || !aligned(ckpt_off, 4) || !aligned(ckpt_pos, 4) || !aligned(dev_status, 4) ||
+      !aligned(workspace, 256))
+    return KDA_ERR_ALIGNMENT;
+  int sms = 0;
+  kda_status st = current_device(&sms);
+  if (st != KDA_OK) return st;
+  const size_t need = kda::prefill_workspace_bytes(n_seq, H, total_tokens, n_segments, sms);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
+  kda::PrefillArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S_in = S_in;
+  a.cu_seqlens = cu_seqlens; a.n_seq = n_seq; a.total_tokens = total_tokens;
+  a.ckpt_off = (ckpt_off && n_ckpt > 0) ? ckpt_off : nullptr;
+  a.ckpt_pos = ckpt_pos; a.n_ckpt = n_ckpt;
+  a.o = o; a.S_out = S_out; a.ckpts = ckpts; a.H = H; a.n_segments = n_segments;
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = dev_status; a.stream = stream;
+  cudaError_t e = kda::launch_prefill(a, sms);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+"""The C-ABI library: it loads, exports what include/kda.h declares, and rejects bad
+arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import kimi_delta_attention_prefill_gb300 as kda
+from kimi_delta_attention_prefill_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA = 0, 1, 2, 3, 4, 5
+HAS_GPU = torch.cuda.is_available()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kda.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"kda_prefill", "kda_decode", "kda_prefill_workspace_size", "kda_status_string"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", kda.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out.stdout, flags=re.M))
+    for n in names:
+        assert n in exported, f"{n} declared in kda.h but not exported"
+        getattr(lib, n)
+
+
+def test_library_does_not_link_the_oracle(lib):
+    out = subprocess.run(["nm", "-D", kda.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    assert "kda_ref_" not in out
+    pkg = os.path.join(ROOT, "kimi_delta_attention_prefill_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "kda_oracle" not in src, f
+
+
+def test_status_strings(lib):
+    assert kda.status_string(0) == "KDA_OK"
+    assert kda.status_string(6) == "KDA_ERR_TIMEOUT"
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+    assert kda.version() >= 100
+
+
+P = lambda a: ctypes.c_void_p(a)
+
+
+def _decode(lib, B=2, n_tok=1, H=3, d=128, q=0x1000, S=0x2000, beta=0x3000, n_commit=None, o=0x4000):
+    return lib.kda_decode(P(q), P(0x5000), P(0x6000), P(0x7000), P(beta), P(S), n_commit, P(o), B, n_tok, H, d,
+                          None, None)
+
+
+def test_decode_host_validation(lib):
+    assert _decode(lib, d=64) == UNSUPPORTED
+    assert _decode(lib, n_tok=0) == UNSUPPORTED
+    assert _decode(lib, n_tok=5) == UNSUPPORTED
+    assert _decode(lib, B=-1) == INVALID
+    assert _decode(lib, B=0) == OK and _decode(lib, H=0) == OK  # empty: no-op
+    assert _decode(lib, q=0) == INVALID
+    assert _decode(lib, S=0) == INVALID
+    assert _decode(lib, q=0x1002) == ALIGNMENT
+    assert _decode(lib, S=0x2008) == ALIGNMENT
+    assert _decode(lib, beta=0x3002) == ALIGNMENT
+    if not HAS_GPU:
+        assert _decode(lib) in (CUDA, UNSUPPORTED)
+
+
+def _prefill(lib, n_seq=1, T=64, H=2, d=128, cu=0x9000, q=0x1000, ckpt_off=None, ckpt_pos=None, n_ckpt=0,
+             ckpts=None, n_segments=0, ws=None, ws_bytes=0):
+    return lib.kda_prefill(P(q), P(0x1100), P(0x1200), P(0x1300), P(0x1400), None, P(cu), n_seq, T,
+                           ckpt_off, ckpt_pos, n_ckpt, P(0x1500), P(0x1600), ckpts, H, d, n_segments, ws,
+                           ws_bytes, None, None)
+
+
+def test_prefill_host_validation(lib):
+    assert _prefill(lib, d=96) == UNSUPPORTED
+    assert _prefill(lib, n_seq=-1) == INVALID
+    assert _prefill(lib, T=-5) == INVALID
+    assert _prefill(lib, n_segments=-1) == INVALID
+    assert _prefill(lib, n_seq=0) == OK and _prefill(lib, H=0) == OK
+    assert _prefill(lib, cu=0) == INVALID
+    assert _prefill(lib, q=0) == INVALID
+    assert _prefill(lib, n_ckpt=3) == INVALID                      # positions without offsets
+    assert _prefill(lib, ckpt_off=P(0xA000), n_ckpt=3) == INVALID  # offsets without positions / slots
+    assert _prefill(lib, q=0x1008) == ALIGNMENT
+    assert _prefill(lib, cu=0x9002) == ALIGNMENT
+    if not HAS_GPU:
+        assert _prefill(lib) in (CUDA, UNSUPPORTED)
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    x = torch.zeros(4, 1, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.decode(x, x, x, x.float(), torch.zeros(4, 1, 2), torch.zeros(4, 2, 128, 128))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(kda, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(kda.KdaLibraryError):
+        kda.library()

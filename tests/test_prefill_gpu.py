@@ -1,0 +1,192 @@
+"""Chunkwise prefill kernel against the fp64 oracle, through the C ABI.
+
+Bar: o within max|o - o_ref| / max|o_ref| <= 1e-2; final state and each checkpoint within
+relative Frobenius error <= 1e-3; checkpoint positions and varlen boundaries bit-exact
+(packed == standalone bit for bit; the checkpoint at len equals S_out bit for bit; no write
+outside a sequence's rows)."""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_prefill_gb300 as kda
+from kimi_delta_attention_prefill_gb300 import inputs
+from kda_gpu_util import O_TOL, S_TOL, host, oracle_units, rel_fro, rel_max, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp, n_segments=0, o_pad=0):
+    d = to_device(inp)
+    T, H = inp.q.shape[0], inp.q.shape[1]
+    o_buf = torch.full((T + 2 * o_pad, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = o_buf[o_pad:o_pad + T]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, S, ck = kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], S_in=d["S0"],
+                           ckpt_off=d["ckpt_off"], ckpt_pos=d["ckpt_pos"], o=o, n_segments=n_segments,
+                           dev_status=status)
+    torch.cuda.synchronize()
+    return o, S, ck, int(status.item()), o_buf
+
+
+def check_against_oracle(inp, o, S, ck, units=None, o_stride=1):
+    n_seq, H = inp.n_seq, inp.q.shape[1]
+    units = units or [(s, h) for s in range(n_seq) for h in range(H)]
+    ref = oracle_units(inp, units, o_stride=o_stride)
+    cu = inp.cu_seqlens.tolist()
+    og, orf, sg, srf, cg, crf = [], [], [], [], [], []
+    for (s, h), r in ref.items():
+        a, b = cu[s], cu[s + 1]
+        og.append(host(o[a:b:o_stride, h]))
+        orf.append(r["o"])
+        sg.append(host(S[s, h]))
+        srf.append(r["S"])
+        if ck is not None and r["ckpts"] is not None and r["ckpts"].shape[0]:
+            lo, hi = int(inp.ckpt_off[s]), int(inp.ckpt_off[s + 1])
+            cg.append(host(ck[lo:hi, h]))
+            crf.append(r["ckpts"])
+    og, orf = np.concatenate(og), np.concatenate(orf)
+    e_o = rel_max(og, orf) if orf.size else 0.0
+    e_s = rel_fro(np.stack(sg), np.stack(srf))
+    assert e_o <= O_TOL, f"o error {e_o:.3e}"
+    assert e_s <= S_TOL, f"state error {e_s:.3e}"
+    for a_, b_ in zip(cg, crf):
+        assert rel_fro(a_, b_) <= S_TOL
+    return e_o, e_s
+
+
+def test_tiny_config():
+    inp = inputs.make_workload("tiny", device="cpu")
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 200, 257])
+@pytest.mark.parametrize("decay", ["sigmoid", "uniform"])
+def test_single_sequence_shapes(T, decay):
+    inp = inputs.make_prefill([T], H=3, seed=100 + T, device="cpu", decay=decay, s0_std=0.02)
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
+
+
+def test_zero_initial_state_and_all_g_at_floor():
+    inp = inputs.make_prefill([300], H=2, seed=7, device="cpu", decay="uniform")
+    inp.g.fill_(inputs.G_MIN)  # every step at the decay floor: the rebasing's worst case
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+    check_against_oracle(inp, o, S, ck)
+
+
+def test_weak_decay_long_memory():
+    inp = inputs.make_prefill([1024], H=2, seed=8, device="cpu", decay="uniform", s0_std=0.02)
+    inp.g.mul_(0.002)  # g in [-0.01, 0): the state remembers hundreds of tokens
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
+
+
+def _varlen_small():
+    lens = [5, 64, 1, 130, 0, 77, 192, 64]
+    inp = inputs.make_prefill(lens, H=4, seed=31, device="cpu", decay="uniform", s0_std=0.02)
+    off, pos = [0], []
+    for n in lens:
+        p = sorted(set(list(range(64, n + 1, 64)) + ([n] if n > 0 else [])))
+        pos += p
+        off.append(len(pos))
+    inp.ckpt_off = torch.tensor(off, dtype=torch.int32)
+    inp.ckpt_pos = torch.tensor(pos, dtype=torch.int32)
+    return inp
+
+
+def test_varlen_checkpoints_and_boundaries():
+    inp = _varlen_small()
+    o, S, ck, st, o_buf = run_gpu(inp, o_pad=64)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
+    # no write outside the packed rows
+    assert torch.isnan(o_buf[:64].float()).all() and torch.isnan(o_buf[-64:].float()).all()
+    assert not torch.isnan(o.float()).any()
+    cu = inp.cu_seqlens.tolist()
+    off = inp.ckpt_off.tolist()
+    pos = inp.ckpt_pos.tolist()
+    for s in range(inp.n_seq):
+        a, b = cu[s], cu[s + 1]
+        # the checkpoint at p = len is the final state, bit for bit
+        if b > a:
+            assert pos[off[s + 1] - 1] == b - a
+            assert torch.equal(ck[off[s + 1] - 1], S[s])
+        # packed == standalone, bit for bit
+        one = inputs.PrefillInputs(inp.q[a:b], inp.k[a:b], inp.v[a:b], inp.g[a:b], inp.beta[a:b],
+                                   inp.S0[s:s + 1], torch.tensor([0, b - a], dtype=torch.int32),
+                                   torch.tensor([0, off[s + 1] - off[s]], dtype=torch.int32),
+                                   torch.tensor(pos[off[s]:off[s + 1]], dtype=torch.int32))
+        o1, S1, ck1, st1, _ = run_gpu(one)
+        assert st1 == 0
+        assert torch.equal(o1, o[a:b])
+        assert torch.equal(S1[0], S[s])
+        if off[s + 1] > off[s]:
+            assert torch.equal(ck1, ck[off[s]:off[s + 1]])
+
+
+def test_restart_from_checkpoint_2560():
+    """Resume at 2560 = 5 x 512 from the checkpoint the kernel wrote; the rest of the run
+    matches the continuous one (bitwise: no segment split)."""
+    T, P = 2800, 2560
+    inp = inputs.make_prefill([T], H=2, seed=41, device="cpu", decay="sigmoid", s0_std=0.02, ckpt_every=512)
+    o, S, ck, st, _ = run_gpu(inp, n_segments=1)
+    assert st == 0
+    assert inp.ckpt_pos.tolist() == [512, 1024, 1536, 2048, 2560]
+    tail = inputs.PrefillInputs(inp.q[P:], inp.k[P:], inp.v[P:], inp.g[P:], inp.beta[P:],
+                                ck[4:5].cpu(), torch.tensor([0, T - P], dtype=torch.int32))
+    o2, S2, _, st2, _ = run_gpu(tail, n_segments=1)
+    assert st2 == 0
+    assert torch.equal(o2, o[P:])
+    assert torch.equal(S2, S)
+
+
+def test_device_side_argument_checks():
+    inp = inputs.make_prefill([64, 64], H=2, seed=5, device="cpu")
+    bad = inputs.PrefillInputs(inp.q, inp.k, inp.v, inp.g, inp.beta, None,
+                               torch.tensor([0, 100, 64], dtype=torch.int32))  # not monotone
+    _, _, _, st, _ = run_gpu(bad)
+    assert st == 7
+    bad2 = inputs.PrefillInputs(inp.q, inp.k, inp.v, inp.g, inp.beta, None, inp.cu_seqlens,
+                                torch.tensor([0, 1, 1], dtype=torch.int32), torch.tensor([30], dtype=torch.int32))
+    _, _, _, st, _ = run_gpu(bad2)
+    assert st == 7  # a checkpoint inside a chunk is not supported
+
+
+def test_prefill_8k_full():
+    """Model-width prefill (1 x 8192 tokens, 96 heads) in the benchmark's launch
+    configuration: every head's final state, and o on every 4th row of every head."""
+    inp = inputs.make_workload("prefill_8k", device="cuda")
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck, o_stride=4)
+
+
+def test_prefill_1m_sampled():
+    """1M-token prefill on 8 heads: two heads against the oracle (final state, o on every
+    64th row); every head finite."""
+    inp = inputs.make_workload("prefill_1m", device="cuda")
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    assert torch.isfinite(S).all()
+    check_against_oracle(inp, o, S, ck, units=[(0, 0), (0, 5)], o_stride=64)
+
+
+def test_varlen_full_sampled():
+    """64 packed sequences, 96 heads, stress decay, nonzero states, checkpoints every 512:
+    12 (sequence, head) units against the oracle, all checkpoint positions bit-exact."""
+    inp = inputs.make_workload("varlen", device="cuda")
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    rng = np.random.default_rng(0)
+    seqs = rng.choice(inp.n_seq, 12, replace=False)
+    units = [(int(s), int(rng.integers(0, inp.q.shape[1]))) for s in seqs]
+    check_against_oracle(inp, o, S, ck, units=units, o_stride=8)
+    off = inp.ckpt_off.tolist()
+    for s in range(inp.n_seq):
+        assert torch.equal(ck[off[s + 1] - 1], S[s]) or (inp.cu_seqlens[s + 1] - inp.cu_seqlens[s]) % 512 != 0
