@@ -64,10 +64,11 @@ constexpr uint32_t SM_XU = 155648;       // X then U (fp16, [t][j], 2 N-panels)
 constexpr uint32_t SM_S = 172032;        // S (fp16, [i][j], 2 N-panels x 128 rows)
 constexpr uint32_t SM_MISC = 204800;
 // inside SM_B after the L/M_qk products are consumed
-constexpr uint32_t SM_W = SM_B;                  // fp32 [64][64]: L, then INV in place
-constexpr uint32_t SM_PT = SM_B + 16384;         // fp32 [16][48] block-row products
-constexpr uint32_t SM_MQK = SM_B + 20480;        // fp16 [64][64] K-major
-constexpr uint32_t SM_INVB = SM_B + 28672;       // fp16 [64][64] K-major
+constexpr uint32_t SM_WL = SM_B;                 // fp32 [64][68]: L (strictly lower, row-scaled by beta)
+constexpr uint32_t SM_WI = SM_B + 17408;         // fp32 [64][68]: INV, built block by block
+constexpr uint32_t SM_PT = SM_B + 34816;         // fp32 4 x [16][16] block scratch (ends at SM_B + 38912)
+constexpr uint32_t SM_INVB = SM_B;               // fp16 [64][64] K-major INV Diag(beta) (over L, once dead)
+constexpr uint32_t SM_MQK = SM_MISC;             // fp16 [64][64] K-major M_qk (over the cumsum scratch)
 __host__ __device__ constexpr uint32_t btb_off(int tb) { return tb == 0 ? 0u : tb == 1 ? 4096u : tb == 2 ? 12288u : 24576u; }
 // misc
 constexpr uint32_t SM_TOT = SM_MISC;             // fp32 [16][128] token-quad sums
@@ -151,6 +152,154 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
     }
   }
   return true;
+}
+
+// ------------------------------------------------------------- INV = (I + L)^-1
+// L is 64 x 64 strictly lower triangular, fp32 in shared memory with row stride kLdw.
+// Block forward substitution over 16 x 16 blocks (D_i = (I + L_ii)^-1):
+//     INV_ii = D_i,   INV_ij = -D_i (L_ij D_j + sum_{j<k<i} L_ik INV_kj)   (i > j)
+// evaluated in dependency stages, one warp per 16 x 16 block product.  The result is
+// scaled by beta along columns and stored as the fp16 K-major operand INV Diag(beta).
+constexpr int kLdw = 68;  // padded row stride (floats): conflict-free float4 row reads
+
+// acc += A * B for 16 x 16 blocks; lane owns row lane / 2, columns 8 (lane % 2) .. +7.
+__device__ __forceinline__ void blk_mac(const float* A, int lda, const float* B, int ldb, float (&acc)[8], int lane) {
+  const int r = lane >> 1, c0 = (lane & 1) * 8;
+  float a[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = *reinterpret_cast<const float4*>(A + r * lda + 4 * q);
+    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float4 b0 = *reinterpret_cast<const float4*>(B + k * ldb + c0);
+    const float4 b1 = *reinterpret_cast<const float4*>(B + k * ldb + c0 + 4);
+    acc[0] += a[k] * b0.x; acc[1] += a[k] * b0.y; acc[2] += a[k] * b0.z; acc[3] += a[k] * b0.w;
+    acc[4] += a[k] * b1.x; acc[5] += a[k] * b1.y; acc[6] += a[k] * b1.z; acc[7] += a[k] * b1.w;
+  }
+}
+__device__ __forceinline__ void blk_load(const float* C, int ldc, float (&acc)[8], int lane) {
+  const int r = lane >> 1, c0 = (lane & 1) * 8;
+  const float4 x = *reinterpret_cast<const float4*>(C + r * ldc + c0);
+  const float4 y = *reinterpret_cast<const float4*>(C + r * ldc + c0 + 4);
+  acc[0] = x.x; acc[1] = x.y; acc[2] = x.z; acc[3] = x.w; acc[4] = y.x; acc[5] = y.y; acc[6] = y.z; acc[7] = y.w;
+}
+__device__ __forceinline__ void blk_store(float* C, int ldc, const float (&acc)[8], int lane, float sign) {
+  const int r = lane >> 1, c0 = (lane & 1) * 8;
+  *reinterpret_cast<float4*>(C + r * ldc + c0) = make_float4(sign * acc[0], sign * acc[1], sign * acc[2], sign * acc[3]);
+  *reinterpret_cast<float4*>(C + r * ldc + c0 + 4) = make_float4(sign * acc[4], sign * acc[5], sign * acc[6], sign * acc[7]);
+}
+__device__ __forceinline__ void blk_copy(const float* S, int lds, float* D, int ldd, int lane) {
+  float acc[8];
+  blk_load(S, lds, acc, lane);
+  blk_store(D, ldd, acc, lane, 1.f);
+}
+
+// All 256 threads call this (it synchronises the CTA).
+__device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const float* beta, uint8_t* invb, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  auto L = [&](int i, int j) { return WL + 16 * i * kLdw + 16 * j; };
+  auto I = [&](int i, int j) { return WI + 16 * i * kLdw + 16 * j; };
+  auto P = [&](int k) { return PT + 256 * k; };
+
+  // diagonal blocks: thread (b, c) solves column c of (I + L_bb) x = e_c
+  if (tid < 64) {
+    const int b = tid >> 4, c = tid & 15;
+    const float* Lb = L(b, b);
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < r; ++m) s += Lb[r * kLdw + m] * x[m];
+      x[r] = (r == c) ? 1.f : (r < c ? 0.f : -s);
+    }
+    float* Db = I(b, b);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Db[r * kLdw + c] = x[r];
+  }
+  __syncthreads();
+  // T_ij = L_ij D_j (stored where INV_ij will go)
+  if (warp < 6) {
+    const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
+    const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    blk_mac(L(i, j), kLdw, I(j, j), kLdw, acc, lane);
+    blk_store(I(i, j), kLdw, acc, lane, 1.f);
+  }
+  __syncthreads();
+  // INV_{i,i-1} = -D_i T_{i,i-1} -> P(i-1)
+  if (warp < 3) {
+    const int i = warp + 1;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    blk_mac(I(i, i), kLdw, I(i, i - 1), kLdw, acc, lane);
+    blk_store(P(i - 1), 16, acc, lane, -1.f);
+  }
+  __syncthreads();
+  // R_20 = T_20 + L_21 INV_10, R_31 = T_31 + L_32 INV_21 (in place); first sub-diagonal into place
+  if (warp < 2) {
+    const int i = warp + 2, j = warp;
+    float acc[8];
+    blk_load(I(i, j), kLdw, acc, lane);
+    blk_mac(L(i, i - 1), kLdw, P(j), 16, acc, lane);
+    blk_store(I(i, j), kLdw, acc, lane, 1.f);
+  } else if (warp < 5) {
+    const int k = warp - 2;
+    blk_copy(P(k), 16, I(k + 1, k), kLdw, lane);
+  }
+  __syncthreads();
+  // INV_20 = -D_2 R_20 -> P(0), INV_31 = -D_3 R_31 -> P(1)
+  if (warp < 2) {
+    const int i = warp + 2, j = warp;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    blk_mac(I(i, i), kLdw, I(i, j), kLdw, acc, lane);
+    blk_store(P(j), 16, acc, lane, -1.f);
+  }
+  __syncthreads();
+  // R_30 = T_30 + L_31 INV_10 + L_32 INV_20 (in place); second sub-diagonal into place
+  if (warp == 0) {
+    float acc[8];
+    blk_load(I(3, 0), kLdw, acc, lane);
+    blk_mac(L(3, 1), kLdw, I(1, 0), kLdw, acc, lane);
+    blk_mac(L(3, 2), kLdw, P(0), 16, acc, lane);
+    blk_store(I(3, 0), kLdw, acc, lane, 1.f);
+  } else if (warp == 1) {
+    blk_copy(P(0), 16, I(2, 0), kLdw, lane);
+  } else if (warp == 2) {
+    blk_copy(P(1), 16, I(3, 1), kLdw, lane);
+  }
+  __syncthreads();
+  // INV_30 = -D_3 R_30 (warp 0, registers); every block -> INV Diag(beta), fp16, K-major [t][s].
+  // The fp16 operand overwrites L, which is no longer read.
+  auto put8 = [&](int t, int g, const float (&v)[8]) {
+    const int s0 = 8 * g;
+    st4(invb + sw128(t, 2 * s0), pack_half2(v[0] * beta[s0], v[1] * beta[s0 + 1]),
+        pack_half2(v[2] * beta[s0 + 2], v[3] * beta[s0 + 3]), pack_half2(v[4] * beta[s0 + 4], v[5] * beta[s0 + 5]),
+        pack_half2(v[6] * beta[s0 + 6], v[7] * beta[s0 + 7]));
+  };
+  if (warp == 0) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    blk_mac(I(3, 3), kLdw, I(3, 0), kLdw, acc, lane);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = -acc[e];
+    put8(48 + (lane >> 1), lane & 1, acc);
+  } else {
+    for (int task = tid - 32; task < 512; task += kThreads - 32) {
+      const int t = task >> 3, g = task & 7;
+      if (t >= 48 && g < 2) continue;  // block (3, 0): warp 0
+      float v[8];
+      if ((g >> 1) > (t >> 4)) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+      } else {
+        const float4 x = *reinterpret_cast<const float4*>(WI + t * kLdw + 8 * g);
+        const float4 y = *reinterpret_cast<const float4*>(WI + t * kLdw + 8 * g + 4);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+      }
+      put8(t, g, v);
+    }
+  }
 }
 
 __device__ __forceinline__ void issue_tile_loads(const KParams& p, uint8_t* sm, uint64_t* bars, int which, int h,
@@ -261,9 +410,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
 
+  // Descriptor bases; per-k-step offsets are added in 16-byte units.
+  const uint64_t dG = smem_desc(smem_u32(sm + SM_G), 16, 1024, kSwizzle128B);     // [QA; KA], K-panel 16384 B
+  const uint64_t dK = smem_desc(smem_u32(sm + SM_K), 16, 1024, kSwizzle128B);     // K_decay, K-panel 8192 B
+  const uint64_t dQ = smem_desc(smem_u32(sm + SM_Q), 16, 1024, kSwizzle128B);     // Q_decay
+  const uint64_t dS = smem_desc(smem_u32(sm + SM_S), 16384, 1024, kSwizzle128B);  // S, MN-major, k-step 2048 B
+  const uint64_t dInv = smem_desc(smem_u32(sm + SM_INVB), 16, 1024, kSwizzle128B);
+  const uint64_t dXU = smem_desc(smem_u32(sm + SM_XU), 8192, 1024, kSwizzle128B);  // MN-major, k-step 2048 B
+  const uint64_t dKR = smem_desc(smem_u32(sm + SM_KR), 8192, 1024, kSwizzle128B);  // MN-major A, k-step 2048 B
+  const uint64_t dMq = smem_desc(smem_u32(sm + SM_MQK), 16, 1024, kSwizzle128B);
+  const uint64_t dB0 = smem_desc(smem_u32(sm + SM_B), 16, 1024, kSwizzle128B);
+
   int ck = w.ck_begin;
   bool aborted = false;
   const int n_chunks = w.c1 - w.c0;
+  float beta_next = 0.f;
+  if (tid < kChunk) {
+    const int64_t r = w.bos + static_cast<int64_t>(w.c0) * kChunk + tid;
+    beta_next = (tid < min(kChunk, w.len - w.c0 * kChunk)) ? p.beta[r * p.H + w.h] : 0.f;
+  }
   for (int n = 0; n < n_chunks && !aborted; ++n) {
     const int cidx = w.c0 + n;
     const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
@@ -273,9 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int64_t row_next = row0 + kChunk;
 
     // ---- 1. inputs of this chunk
+    if (tid < kChunk) {
+      s_beta[tid] = beta_next;
+      const int vn = has_next ? min(kChunk, w.len - (cidx + 1) * kChunk) : 0;
+      beta_next = tid < vn ? p.beta[(row_next + tid) * p.H + w.h] : 0.f;
+    }
     bool ok = mbar_wait(&bars[BAR_IN], n & 1) && mbar_wait(&bars[BAR_V0 + vstage], (n >> 1) & 1);
     if (!ok) { if (tid == 0) ctrl[1] = 1; }
-    if (tid < kChunk) s_beta[tid] = tid < valid ? p.beta[(row0 + tid) * p.H + w.h] : 0.f;
     if (tid == 0 && ok && has_next) {
       mbar_arrive_expect_tx(&bars[BAR_V0 + (vstage ^ 1)], 16384);
       issue_tile_loads(p, sm, bars, 8, w.h, row_next, vstage ^ 1);
@@ -299,17 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int e = 0; e < 8; ++e) G[u][e] += G[u - 1][e];
       float* tot = reinterpret_cast<float*>(sm + SM_TOT);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) tot[tq * 128 + cg * 8 + e] = G[3][e];
+      *reinterpret_cast<float4*>(tot + tq * 128 + cg * 8) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
+      *reinterpret_cast<float4*>(tot + tq * 128 + cg * 8 + 4) = make_float4(G[3][4], G[3][5], G[3][6], G[3][7]);
     }
     __syncthreads();
     if (ctrl[1]) { aborted = true; break; }
     {
       const float* tot = reinterpret_cast<const float*>(sm + SM_TOT);
       float off[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int j = 0; j < tq; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) off[e] += tot[j * 128 + cg * 8 + e];
+      for (int j = 0; j < tq; ++j) {
+        const float4 a = *reinterpret_cast<const float4*>(tot + j * 128 + cg * 8);
+        const float4 b = *reinterpret_cast<const float4*>(tot + j * 128 + cg * 8 + 4);
+        off[0] += a.x; off[1] += a.y; off[2] += a.z; off[3] += a.w;
+        off[4] += b.x; off[5] += b.y; off[6] += b.z; off[7] += b.w;
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -335,17 +507,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         float* rt = reinterpret_cast<float*>(sm + SM_RT);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          at[b * 128 + i] = expf(gb[b * 128 + i]);
-          rt[b * 128 + i] = expf(gl - gb[b * 128 + i]);
+          at[b * 128 + i] = __expf(gb[b * 128 + i]);
+          rt[b * 128 + i] = __expf(gl - gb[b * 128 + i]);
         }
-        reinterpret_cast<float*>(sm + SM_AL)[i] = expf(gl);
+        reinterpret_cast<float*>(sm + SM_AL)[i] = __expf(gl);
       } else {
         float* f = reinterpret_cast<float*>(sm + SM_F);
         int idx = 0;
 #pragma unroll
         for (int b = 1; b < 4; ++b)
 #pragma unroll
-          for (int s = 0; s < b; ++s, ++idx) f[idx * 128 + i] = expf(gb[b * 128 + i] - gb[s * 128 + i]);
+          for (int s = 0; s < b; ++s, ++idx) f[idx * 128 + i] = __expf(gb[b * 128 + i] - gb[s * 128 + i]);
       }
     }
     __syncthreads();
@@ -355,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const float* rt = reinterpret_cast<const float*>(sm + SM_RT) + tb * 128 + cg * 8;
       const float* fp = reinterpret_cast<const float*>(sm + SM_F);
       const int kpanel = cg >> 3, kchunk = cg & 7;
+      float gbr[8], atr[8], rtr[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { gbr[e] = gb[e]; atr[e] = at[e]; rtr[e] = rt[e]; }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = tq * 4 + u;
@@ -369,14 +544,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float kk = m ? kf[e] : 0.f;
-          const float E = expf(G[u][e] - gb[e]);  // <= 1
-          const float Ei = 1.0f / E;               // in [1, e^75]
+          const float x = G[u][e] - gbr[e];   // <= 0, >= -75
+          const float E = __expf(x);
+          const float Ei = __expf(-x);
           qa[e] = qf[e] * E;
           ka[e] = kk * E;
-          qd[e] = qa[e] * at[e];
-          kd[e] = ka[e] * at[e];
+          qd[e] = qa[e] * atr[e];
+          kd[e] = ka[e] * atr[e];
           kb[e] = kk * Ei;
-          kr[e] = kb[e] * rt[e];
+          kr[e] = kb[e] * rtr[e];
         }
         st4(qp, pack_half2(qd[0], qd[1]), pack_half2(qd[2], qd[3]), pack_half2(qd[4], qd[5]), pack_half2(qd[6], qd[7]));
         st4(kp, pack_half2(kd[0], kd[1]), pack_half2(kd[2], kd[3]), pack_half2(kd[4], kd[5]), pack_half2(kd[6], kd[7]));
@@ -411,28 +587,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // ---- 3. L / M_qk products (bf16) and K_decay S (fp16)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t a_base = smem_u32(sm + SM_G);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const uint32_t rows = 16u * (b + 1);
-        const uint32_t b_base = smem_u32(sm + SM_B + btb_off(b));
         const uint32_t idesc = idesc_f16(128, rows, true, false, false);
+        const uint64_t db = dB0 + (btb_off(b) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = smem_desc(a_base + (kk >> 2) * 16384 + 32 * (kk & 3), 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(b_base + (kk >> 2) * rows * 128 + 32 * (kk & 3), 16, 1024, kSwizzle128B);
+          const uint64_t ad = dG + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4);
+          const uint64_t bd = db + (((kk >> 2) * rows * 128 + 32 * (kk & 3)) >> 4);
           mma_f16(tmem + kTLM + lm_col(b), ad, bd, idesc, kk > 0);
         }
       }
       mma_commit(&bars[BAR_LM]);
-      const uint32_t kd_base = smem_u32(sm + SM_K), s_base = smem_u32(sm + SM_S);
       const uint32_t idesc = idesc_f16(64, 128, false, false, true);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(kd_base + (kk >> 2) * 8192 + 32 * (kk & 3), 16, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(s_base + kk * 2048, 16384, 1024, kSwizzle128B);
-        mma_f16(tmem + kTP, ad, bd, idesc, kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tmem + kTP, dK + (((kk >> 2) * 8192 + 32 * (kk & 3)) >> 4), dS + ((kk * 2048) >> 4), idesc, kk > 0);
       mma_commit(&bars[BAR_P]);
     }
 
@@ -440,20 +611,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     {
       const int i = quarter * 32 + lane;
       const float al = reinterpret_cast<const float*>(sm + SM_AL)[i];
+      float r[4][16];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTS + hcol * 64 + m * 16, r[m]);
+      tmem_wait_ld();
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        float r[16];
-        const uint32_t a = tmem + tl + kTS + hcol * 64 + m * 16;
-        tmem_ld16(a, r);
-        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] *= al;
-        tmem_st16(a, r);
+        for (int e = 0; e < 16; ++e) r[m][e] *= al;
+        tmem_st16(tmem + tl + kTS + hcol * 64 + m * 16, r[m]);
       }
       tmem_wait_st();
     }
 
-    // ---- 5. read L and M_qk
+    // ---- 5. read L and M_qk (row block tb reads the accumulator built with B_tb)
     ok = mbar_wait(&bars[BAR_LM], n & 1);
     if (!ok && tid == 0) ctrl[1] = 1;
     tc_fence_after();
@@ -462,24 +633,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const bool is_l = quarter >= 2;
       const int t = (quarter & 1) * 32 + lane;
       const int tbl = t >> 4;
-      const int g0 = (quarter & 1) ? 3 : 0, g1 = (quarter & 1) ? 10 : 3;  // 16-col groups of this warp
+      const int g0 = (quarter & 1) ? 3 : 0, ng = (quarter & 1) ? 7 : 3;  // 16-column groups of this warp
+      const int lo = static_cast<int>(lm_col(tbl)), hi = lo + 16 * (tbl + 1);
       const float bt = s_beta[t];
-      for (int grp = g0; grp < g1; ++grp) {
-        float r[16];
-        tmem_ld16(tmem + tl + kTLM + grp * 16, r);
-        tmem_wait_ld();
-        const int col = grp * 16;
-        const int lo = static_cast<int>(lm_col(tbl)), hi = lo + 16 * (tbl + 1);
-        if (col < lo || col >= hi) continue;
+      float r[7][16];
+#pragma unroll
+      for (int gi = 0; gi < 7; ++gi)
+        if (gi < ng) tmem_ld16(tmem + tl + kTLM + (g0 + gi) * 16, r[gi]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int gi = 0; gi < 7; ++gi) {
+        const int col = (g0 + gi) * 16;
+        if (gi >= ng || col < lo || col >= hi) continue;
         const int s0 = col - lo;  // s block start
         if (is_l) {
-          float* wr = reinterpret_cast<float*>(sm + SM_W) + t * 64 + s0;
+          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + s0;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) wr[e] = (s0 + e < t) ? bt * r[e] : 0.f;
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(wr + e) =
+                make_float4((s0 + e < t) ? bt * r[gi][e] : 0.f, (s0 + e + 1 < t) ? bt * r[gi][e + 1] : 0.f,
+                            (s0 + e + 2 < t) ? bt * r[gi][e + 2] : 0.f, (s0 + e + 3 < t) ? bt * r[gi][e + 3] : 0.f);
         } else {
           float v[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = (s0 + e <= t) ? r[e] : 0.f;
+          for (int e = 0; e < 16; ++e) v[e] = (s0 + e <= t) ? r[gi][e] : 0.f;
           uint8_t* mp = sm + SM_MQK;
           st4(mp + sw128(t, 2 * s0), pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
               pack_half2(v[6], v[7]));
@@ -490,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // zero the s blocks past this row's block
       for (int sb = tbl + 1; sb < 4; ++sb) {
         if (is_l) {
-          float* wr = reinterpret_cast<float*>(sm + SM_W) + t * 64 + sb * 16;
+          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + sb * 16;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) wr[e] = 0.f;
+          for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(wr + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
           uint8_t* mp = sm + SM_MQK;
           st4(mp + sw128(t, 32 * sb), 0, 0, 0, 0);
@@ -512,67 +689,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_arrive_expect_tx(&bars[BAR_IN], 65536);
         issue_tile_loads(p, sm, bars, 4, w.h, row_next, 0);
       }
-      const uint32_t qd_base = smem_u32(sm + SM_Q), s_base = smem_u32(sm + SM_S);
       const uint32_t idesc = idesc_f16(64, 128, false, false, true);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(qd_base + (kk >> 2) * 8192 + 32 * (kk & 3), 16, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(s_base + kk * 2048, 16384, 1024, kSwizzle128B);
-        mma_f16(tmem + kTO, ad, bd, idesc, kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tmem + kTO, dQ + (((kk >> 2) * 8192 + 32 * (kk & 3)) >> 4), dS + ((kk * 2048) >> 4), idesc, kk > 0);
     }
 
-    // ---- 7. INV = (I + L)^-1 in fp32, blocked by 16 (in place in W), then INV Diag(beta)
-    {
-      float* W = reinterpret_cast<float*>(sm + SM_W);
-      if (warp < 4 && lane < 16) {  // diagonal block `warp`, column `lane`
-        const int b0 = warp * 16, c = lane;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float s = 0.f;
-#pragma unroll
-          for (int m = 0; m < r; ++m) s += W[(b0 + r) * 64 + b0 + m] * x[m];
-          x[r] = (r == c) ? 1.f : (r < c ? 0.f : -s);
-        }
-        __syncwarp(0x0000ffffu);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) W[(b0 + r) * 64 + b0 + c] = x[r];
-      }
-      __syncthreads();
-      float* PT = reinterpret_cast<float*>(sm + SM_PT);
-      const int r = tid >> 4, cb = tid & 15;
-      for (int ib = 1; ib < 4; ++ib) {
-        const int ncol = 16 * ib;
-        // P = L[ib, 0:ib] * INV[0:ib, 0:ib]
-        for (int c = cb; c < ncol; c += 16) {
-          float s = 0.f;
-          for (int k2 = c; k2 < ncol; ++k2) s += W[(ncol + r) * 64 + k2] * W[k2 * 64 + c];
-          PT[r * 48 + c] = s;
-        }
-        __syncthreads();
-        // INV[ib, 0:ib] = -D_ib P
-        for (int c = cb; c < ncol; c += 16) {
-          float s = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; ++m) s += W[(ncol + r) * 64 + ncol + m] * PT[m * 48 + c];
-          W[(ncol + r) * 64 + c] = -s;
-        }
-        __syncthreads();
-      }
-      // INV Diag(beta) -> fp16 K-major operand
-      {
-        const int t = tid >> 2, sg = tid & 3;
-        float v[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = W[t * 64 + sg * 16 + e] * s_beta[sg * 16 + e];
-        uint8_t* ip = sm + SM_INVB;
-        st4(ip + sw128(t, 32 * sg), pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
-            pack_half2(v[6], v[7]));
-        st4(ip + sw128(t, 32 * sg + 16), pack_half2(v[8], v[9]), pack_half2(v[10], v[11]), pack_half2(v[12], v[13]),
-            pack_half2(v[14], v[15]));
-      }
-    }
+    // ---- 7. INV = (I + L)^-1 in fp32 by 16 x 16 blocks, then INV Diag(beta) as fp16
+    invert_unit_lower(reinterpret_cast<float*>(sm + SM_WL), reinterpret_cast<float*>(sm + SM_WI),
+                      reinterpret_cast<float*>(sm + SM_PT), s_beta, sm + SM_INVB, tid);
 
     // ---- 8. X = V - K_decay S  (rows past the sequence end are zero)
     ok = mbar_wait(&bars[BAR_P], n & 1);
@@ -582,19 +707,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int t = quarter * 16 + (lane & 15);
       const uint8_t* vt = sm + SM_V + vstage * 16384 + hcol * 8192;
       uint8_t* xp = sm + SM_XU + hcol * 8192;
+      float r[4][16];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float r[16];
-        tmem_ld16(tmem + tl + kTP + hcol * 64 + m * 16, r);
-        tmem_wait_ld();
-        if (lane < 16) {
+      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTP + hcol * 64 + m * 16, r[m]);
+      tmem_wait_ld();
+      if (lane < 16) {
+        const bool mk = t < valid;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
           float v0[8], v1[8];
           bf16x8_to_f32(*reinterpret_cast<const uint4*>(vt + sw128(t, 32 * m)), v0);
           bf16x8_to_f32(*reinterpret_cast<const uint4*>(vt + sw128(t, 32 * m + 16)), v1);
-          const bool mk = t < valid;
           float x[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) { x[e] = mk ? v0[e] - r[e] : 0.f; x[8 + e] = mk ? v1[e] - r[8 + e] : 0.f; }
+          for (int e = 0; e < 8; ++e) { x[e] = mk ? v0[e] - r[m][e] : 0.f; x[8 + e] = mk ? v1[e] - r[m][8 + e] : 0.f; }
           st4(xp + sw128(t, 32 * m), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
               pack_half2(x[6], x[7]));
           st4(xp + sw128(t, 32 * m + 16), pack_half2(x[8], x[9]), pack_half2(x[10], x[11]), pack_half2(x[12], x[13]),
@@ -611,14 +737,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (tid == 0) {
       tc_fence_after();
       if (has_next) issue_tile_loads(p, sm, bars, 2, w.h, row_next, 0);
-      const uint32_t a_base = smem_u32(sm + SM_INVB), b_base = smem_u32(sm + SM_XU);
       const uint32_t idesc = idesc_f16(64, 128, false, false, true);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(b_base + kk * 2048, 8192, 1024, kSwizzle128B);
-        mma_f16(tmem + kTP, ad, bd, idesc, kk > 0);
-      }
+      for (int kk = 0; kk < 4; ++kk) mma_f16(tmem + kTP, dInv + ((32 * kk) >> 4), dXU + ((kk * 2048) >> 4), idesc, kk > 0);
       mma_commit(&bars[BAR_U]);
     }
 
@@ -629,19 +750,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     {
       const int t = quarter * 16 + (lane & 15);
       uint8_t* up = sm + SM_XU + hcol * 8192;
+      float r[4][16];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float r[16];
-        tmem_ld16(tmem + tl + kTP + hcol * 64 + m * 16, r);
-        tmem_wait_ld();
-        if (lane < 16) {
-          const bool mk = t < valid;
+      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTP + hcol * 64 + m * 16, r[m]);
+      tmem_wait_ld();
+      if (lane < 16) {
+        const bool mk = t < valid;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = mk ? r[e] : 0.f;
-          st4(up + sw128(t, 32 * m), pack_half2(r[0], r[1]), pack_half2(r[2], r[3]), pack_half2(r[4], r[5]),
-              pack_half2(r[6], r[7]));
-          st4(up + sw128(t, 32 * m + 16), pack_half2(r[8], r[9]), pack_half2(r[10], r[11]), pack_half2(r[12], r[13]),
-              pack_half2(r[14], r[15]));
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[m][e] = mk ? r[m][e] : 0.f;
+          st4(up + sw128(t, 32 * m), pack_half2(r[m][0], r[m][1]), pack_half2(r[m][2], r[m][3]),
+              pack_half2(r[m][4], r[m][5]), pack_half2(r[m][6], r[m][7]));
+          st4(up + sw128(t, 32 * m + 16), pack_half2(r[m][8], r[m][9]), pack_half2(r[m][10], r[m][11]),
+              pack_half2(r[m][12], r[m][13]), pack_half2(r[m][14], r[m][15]));
         }
       }
     }
@@ -654,14 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (tid == 0) {
       tc_fence_after();
       if (has_next) issue_tile_loads(p, sm, bars, 1, w.h, row_next, 0);
-      const uint32_t kr_base = smem_u32(sm + SM_KR), u_base = smem_u32(sm + SM_XU), mq_base = smem_u32(sm + SM_MQK);
       const uint32_t id_s = idesc_f16(128, 128, false, true, true);
       const uint32_t id_o = idesc_f16(64, 128, false, false, true);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ud = smem_desc(u_base + kk * 2048, 8192, 1024, kSwizzle128B);
-        mma_f16(tmem + kTS, smem_desc(kr_base + kk * 2048, 8192, 1024, kSwizzle128B), ud, id_s, 1);
-        mma_f16(tmem + kTO, smem_desc(mq_base + 32 * kk, 16, 1024, kSwizzle128B), ud, id_o, 1);
+        const uint64_t ud = dXU + ((kk * 2048) >> 4);
+        mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_s, 1);
+        mma_f16(tmem + kTO, dMq + ((32 * kk) >> 4), ud, id_o, 1);
       }
       mma_commit(&bars[BAR_S]);
     }
@@ -674,16 +795,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int t = quarter * 16 + (lane & 15);
       const bool wr = lane < 16 && t < valid;
       __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim + hcol * 64;
+      float r[4][16];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float r[16];
-        tmem_ld16(tmem + tl + kTO + hcol * 64 + m * 16, r);
-        tmem_wait_ld();
-        if (wr) {
+      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTO + hcol * 64 + m * 16, r[m]);
+      tmem_wait_ld();
+      if (wr) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
           uint4* dst = reinterpret_cast<uint4*>(orow + m * 16);
-          dst[0] = make_uint4(pack_bf162(r[0], r[1]), pack_bf162(r[2], r[3]), pack_bf162(r[4], r[5]), pack_bf162(r[6], r[7]));
-          dst[1] = make_uint4(pack_bf162(r[8], r[9]), pack_bf162(r[10], r[11]), pack_bf162(r[12], r[13]),
-                              pack_bf162(r[14], r[15]));
+          dst[0] = make_uint4(pack_bf162(r[m][0], r[m][1]), pack_bf162(r[m][2], r[m][3]), pack_bf162(r[m][4], r[m][5]),
+                              pack_bf162(r[m][6], r[m][7]));
+          dst[1] = make_uint4(pack_bf162(r[m][8], r[m][9]), pack_bf162(r[m][10], r[m][11]),
+                              pack_bf162(r[m][12], r[m][13]), pack_bf162(r[m][14], r[m][15]));
         }
       }
     }
@@ -697,25 +820,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
       const int i = quarter * 32 + lane;
       uint8_t* dst = sm + SM_S + hcol * 16384;
+      float r[4][16];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTS + hcol * 64 + m * 16, r[m]);
+      tmem_wait_ld();
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        float r[16];
         const int c = hcol * 64 + m * 16;
-        tmem_ld16(tmem + tl + kTS + c, r);
-        tmem_wait_ld();
-        st4(dst + sw128(i, 32 * m), pack_half2(r[0], r[1]), pack_half2(r[2], r[3]), pack_half2(r[4], r[5]),
-            pack_half2(r[6], r[7]));
-        st4(dst + sw128(i, 32 * m + 16), pack_half2(r[8], r[9]), pack_half2(r[10], r[11]), pack_half2(r[12], r[13]),
-            pack_half2(r[14], r[15]));
+        st4(dst + sw128(i, 32 * m), pack_half2(r[m][0], r[m][1]), pack_half2(r[m][2], r[m][3]),
+            pack_half2(r[m][4], r[m][5]), pack_half2(r[m][6], r[m][7]));
+        st4(dst + sw128(i, 32 * m + 16), pack_half2(r[m][8], r[m][9]), pack_half2(r[m][10], r[m][11]),
+            pack_half2(r[m][12], r[m][13]), pack_half2(r[m][14], r[m][15]));
         if (ckdst) {
           float4* d4 = reinterpret_cast<float4*>(ckdst + i * kHeadDim + c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) d4[e] = make_float4(r[m][4 * e], r[m][4 * e + 1], r[m][4 * e + 2], r[m][4 * e + 3]);
         }
         if (fin) {
           float4* d4 = reinterpret_cast<float4*>(fin + i * kHeadDim + c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) d4[e] = make_float4(r[m][4 * e], r[m][4 * e + 1], r[m][4 * e + 2], r[m][4 * e + 3]);
         }
       }
     }
