@@ -93,6 +93,7 @@ kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, 
   if (n_seq < 0 || H < 0 || total_tokens < 0 || n_ckpt < 0 || n_segments < 0) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0x7fffffffLL || static_cast<int64_t>(n_seq) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
   if (n_seq == 0 || H == 0) return KDA_OK;
+  if (H > 65535) return KDA_ERR_UNSUPPORTED;  // heads index the grid's y dimension
   if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
   if (ckpt_off == nullptr && n_ckpt != 0) return KDA_ERR_INVALID_ARG;

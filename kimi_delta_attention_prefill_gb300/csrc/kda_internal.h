@@ -44,8 +44,80 @@ struct PrefillArgs {
   cudaStream_t stream;
 };
 
+// ----------------------------------------------------------------- sequence split
+// Planner rule ("部署 Kimi K3 ..." section 1.2: split a sequence over the SMs when its
+// rank holds few heads).  A function of the sequence's own length, H, the SM count and
+// the caller's request only, so a sequence is split the same way packed or alone.
+//   n_segments > 0 : min(n_segments, chunks)
+//   n_segments = 0 : min(num_sms / H, chunks / kMinSegChunks), at least 1
+constexpr int kMinSegChunks = 64;  // segments shorter than 4096 tokens do not pay for the extra passes
+
+__host__ __device__ inline int plan_segments(int len, int H, int num_sms, int n_segments) {
+  const int nch = (len + kChunk - 1) / kChunk;
+  if (nch <= 1) return 1;
+  if (n_segments > 0) return n_segments < nch ? n_segments : nch;
+  const int target = num_sms / (H > 0 ? H : 1);
+  const int by_len = nch / kMinSegChunks;
+  const int n = target < by_len ? target : by_len;
+  return n < 1 ? 1 : n;
+}
+
+// Work-item modes of the prefill kernel.
+enum : int {
+  kModeFull = 0,   // whole sequence from S_in: outputs, checkpoints, S_out
+  kModeFirst = 1,  // first segment from S_in: outputs, checkpoints, exit state -> slot A
+  kModeZero = 2,   // middle segment from a zero state, no outputs: S~ -> slot A
+  kModeTrans = 3,  // middle segment from the identity with V = 0: M -> slot B
+  kModeTail = 4    // segment 1.. from the entry state in slot C: outputs, checkpoints, S_out if last
+};
+
+// Workspace of the split path (all offsets 256-byte aligned):
+//   [0, 256)       int counts[2]  (pass-1 items, pass-3 items)
+//   items1[max1]   int4 {seq, chunk begin, chunk end, mode | slot << 3}
+//   items3[max3]   int4
+//   seginfo[n_seq] int2 {first slot, segment count}
+//   slots          [n_slots][H][3][128][128] fp32 (A: exit or S~, B: M, C: entry)
+struct SplitLayout {
+  int64_t extra = 0;  // bound on the total number of extra segments (0: no split)
+  int64_t max1 = 0, max3 = 0, n_slots = 0;
+  size_t off_items1 = 0, off_items3 = 0, off_seginfo = 0, off_slots = 0, bytes = 0;
+};
+
+__host__ inline SplitLayout split_layout(int n_seq, int H, int64_t total_tokens, int n_segments, int num_sms) {
+  SplitLayout L;
+  int64_t extra = 0;
+  if (n_segments > 1) {
+    const int64_t a = static_cast<int64_t>(n_seq) * (n_segments - 1);
+    const int64_t b = total_tokens / kChunk + n_seq;
+    extra = a < b ? a : b;
+  } else if (n_segments == 0) {
+    const int target = num_sms / (H > 0 ? H : 1);
+    if (target >= 2) {
+      const int64_t a = static_cast<int64_t>(n_seq) * (target - 1);
+      const int64_t b = total_tokens / (static_cast<int64_t>(kChunk) * kMinSegChunks);
+      extra = a < b ? a : b;
+    }
+  }
+  if (extra <= 0) return L;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  L.extra = extra;
+  L.max1 = n_seq + 2 * extra;
+  L.max3 = extra;
+  L.n_slots = (2 * extra < n_seq + extra) ? 2 * extra : n_seq + extra;
+  L.off_items1 = 256;
+  L.off_items3 = up(L.off_items1 + 16 * static_cast<size_t>(L.max1));
+  L.off_seginfo = up(L.off_items3 + 16 * static_cast<size_t>(L.max3));
+  L.off_slots = up(L.off_seginfo + 8 * static_cast<size_t>(n_seq));
+  L.bytes = L.off_slots + static_cast<size_t>(L.n_slots) * H * 3 * kHeadDim * kHeadDim * sizeof(float);
+  return L;
+}
+
 // Workspace bytes for the segment split; 0 when it cannot be taken.
 size_t prefill_workspace_bytes(int n_seq, int H, int64_t total_tokens, int n_segments, int num_sms);
 cudaError_t launch_prefill(const PrefillArgs& a, int num_sms);
+
+// The split path's helper kernels (kda_segment.cu).
+cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, int num_sms);
+cudaError_t launch_split_scan(const PrefillArgs& a, const SplitLayout& L);
 
 }  // namespace kda

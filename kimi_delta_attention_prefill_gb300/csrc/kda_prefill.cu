@@ -111,6 +111,9 @@ struct KParams {
   int n_seq, H;
   int64_t total_tokens;
   int64_t n_ckpt;
+  const int4* items;      // work items (split path) or nullptr: item x = whole sequence x
+  const int* item_count;  // device count of valid items
+  float* slots;           // split-path state slots [slot][H][3][128][128]
 };
 
 __device__ __forceinline__ float4 ld4(const uint8_t* p) { return *reinterpret_cast<const float4*>(p); }
@@ -332,10 +335,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, hcol = warp >> 2;
 
-  // ---- work item (no split: one CTA per (sequence, head))
+  // ---- work item: (sequence, head, chunk range, mode)
+  int4 it;
+  if (p.items) {
+    if (static_cast<int>(blockIdx.x) >= *p.item_count) return;
+    it = p.items[blockIdx.x];
+  } else {
+    it = make_int4(static_cast<int>(blockIdx.x), 0, -1, kModeFull);
+  }
+  const int mode = it.w & 7, slot = it.w >> 3;
   Work w;
-  w.seq = blockIdx.x / p.H;
-  w.h = blockIdx.x - w.seq * p.H;
+  w.seq = it.x;
+  w.h = blockIdx.y;
   if (tid == 0) {
     int64_t bos; int len, cb, ce;
     const bool ok = check_sequence(p, w.seq, bos, len, cb, ce);
@@ -344,16 +355,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
   __syncthreads();
   if (!ctrl[2]) return;
+  const bool do_o = mode == kModeFull || mode == kModeFirst || mode == kModeTail;
+  const bool v_zero = mode == kModeTrans, entry_identity = mode == kModeTrans;
   {
     const int64_t a = p.cu[w.seq], b = p.cu[w.seq + 1];
+    const int64_t unit = static_cast<int64_t>(w.seq) * p.H + w.h;
+    auto slot_buf = [&](int buf) { return p.slots + ((static_cast<int64_t>(slot) * p.H + w.h) * 3 + buf) * (kHeadDim * kHeadDim); };
     w.bos = a;
     w.len = static_cast<int>(b - a);
-    w.c0 = 0;
-    w.c1 = (w.len + kChunk - 1) / kChunk;
-    w.entry = p.S_in ? p.S_in + (static_cast<int64_t>(w.seq) * p.H + w.h) * (kHeadDim * kHeadDim) : nullptr;
-    w.s_out = p.S_out ? p.S_out + (static_cast<int64_t>(w.seq) * p.H + w.h) * (kHeadDim * kHeadDim) : nullptr;
-    w.ck_begin = p.ckpt_off ? p.ckpt_off[w.seq] : 0;
-    w.ck_end = p.ckpt_off ? p.ckpt_off[w.seq + 1] : 0;
+    const int nch = (w.len + kChunk - 1) / kChunk;
+    w.c0 = it.y;
+    w.c1 = it.z < 0 ? nch : it.z;
+    float* s_out = p.S_out ? p.S_out + unit * (kHeadDim * kHeadDim) : nullptr;
+    const float* s_in = p.S_in ? p.S_in + unit * (kHeadDim * kHeadDim) : nullptr;
+    switch (mode) {
+      case kModeFirst: w.entry = s_in; w.s_out = slot_buf(0); break;
+      case kModeZero: w.entry = nullptr; w.s_out = slot_buf(0); break;
+      case kModeTrans: w.entry = nullptr; w.s_out = slot_buf(1); break;
+      case kModeTail: w.entry = slot_buf(2); w.s_out = (w.c1 == nch) ? s_out : nullptr; break;
+      default: w.entry = s_in; w.s_out = s_out; break;
+    }
+    w.ck_begin = w.ck_end = 0;
+    if (do_o && p.ckpt_off) {
+      w.ck_end = p.ckpt_off[w.seq + 1];
+      int j = p.ckpt_off[w.seq];
+      while (j < w.ck_end && p.ckpt_pos[j] <= w.c0 * kChunk) ++j;
+      w.ck_begin = j;
+    }
   }
 
   // ---- empty sequence: the final state is the entry state
@@ -395,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int e = 0; e < 16; e += 4) {
         float4 v4 = w.entry ? *reinterpret_cast<const float4*>(w.entry + i * kHeadDim + c + e) : make_float4(0, 0, 0, 0);
+        if (entry_identity)
+          v4 = make_float4(i == c + e ? 1.f : 0.f, i == c + e + 1 ? 1.f : 0.f, i == c + e + 2 ? 1.f : 0.f,
+                           i == c + e + 3 ? 1.f : 0.f);
         r[e] = v4.x; r[e + 1] = v4.y; r[e + 2] = v4.z; r[e + 3] = v4.w;
       }
       tmem_st16(tmem + tl + kTS + c, r);
@@ -689,10 +720,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_arrive_expect_tx(&bars[BAR_IN], 65536);
         issue_tile_loads(p, sm, bars, 4, w.h, row_next, 0);
       }
-      const uint32_t idesc = idesc_f16(64, 128, false, false, true);
+      if (do_o) {
+        const uint32_t idesc = idesc_f16(64, 128, false, false, true);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_f16(tmem + kTO, dQ + (((kk >> 2) * 8192 + 32 * (kk & 3)) >> 4), dS + ((kk * 2048) >> 4), idesc, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16(tmem + kTO, dQ + (((kk >> 2) * 8192 + 32 * (kk & 3)) >> 4), dS + ((kk * 2048) >> 4), idesc, kk > 0);
+      }
     }
 
     // ---- 7. INV = (I + L)^-1 in fp32 by 16 x 16 blocks, then INV Diag(beta) as fp16
@@ -720,7 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           bf16x8_to_f32(*reinterpret_cast<const uint4*>(vt + sw128(t, 32 * m + 16)), v1);
           float x[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) { x[e] = mk ? v0[e] - r[m][e] : 0.f; x[8 + e] = mk ? v1[e] - r[m][8 + e] : 0.f; }
+          for (int e = 0; e < 8; ++e) {
+            x[e] = mk ? (v_zero ? 0.f : v0[e]) - r[m][e] : 0.f;
+            x[8 + e] = mk ? (v_zero ? 0.f : v1[e]) - r[m][8 + e] : 0.f;
+          }
           st4(xp + sw128(t, 32 * m), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
               pack_half2(x[6], x[7]));
           st4(xp + sw128(t, 32 * m + 16), pack_half2(x[8], x[9]), pack_half2(x[10], x[11]), pack_half2(x[12], x[13]),
@@ -782,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t ud = dXU + ((kk * 2048) >> 4);
         mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_s, 1);
-        mma_f16(tmem + kTO, dMq + ((32 * kk) >> 4), ud, id_o, 1);
+        if (do_o) mma_f16(tmem + kTO, dMq + ((32 * kk) >> 4), ud, id_o, 1);
       }
       mma_commit(&bars[BAR_S]);
     }
@@ -793,12 +829,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     {
       const int t = quarter * 16 + (lane & 15);
-      const bool wr = lane < 16 && t < valid;
+      const bool wr = do_o && lane < 16 && t < valid;
       __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim + hcol * 64;
       float r[4][16];
+      if (do_o) {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTO + hcol * 64 + m * 16, r[m]);
-      tmem_wait_ld();
+        for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTO + hcol * 64 + m * 16, r[m]);
+        tmem_wait_ld();
+      }
       if (wr) {
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -893,15 +931,10 @@ bool make_map(CUtensorMap* m, const void* base, bool is_f32, int H, int64_t T) {
 }  // namespace
 
 size_t prefill_workspace_bytes(int n_seq, int H, int64_t total_tokens, int n_segments, int num_sms) {
-  (void)n_seq; (void)H; (void)total_tokens; (void)n_segments; (void)num_sms;
-  return 0;
+  return split_layout(n_seq, H, total_tokens, n_segments, num_sms).bytes;
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
-  (void)num_sms;
-  if (a.total_tokens == 0) {
-    // every sequence is empty: final states are the entry states
-  }
   KParams p;
   memset(&p, 0, sizeof(p));
   const int64_t T = a.total_tokens;
@@ -919,8 +952,28 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.n_seq) * a.H);
-  prefill_kernel<<<grid, kThreads, kSmemAlloc, a.stream>>>(p);
+  const SplitLayout L = split_layout(a.n_seq, a.H, T, a.n_segments, num_sms);
+  if (L.extra == 0) {
+    // one CTA per (sequence, head), whole sequence
+    prefill_kernel<<<dim3(static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
+                     a.stream>>>(p);
+    return cudaGetLastError();
+  }
+  // sequence split: plan, pass 1 (first segments + (S~, M) of middle segments), scan, pass 3
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  cudaError_t e = launch_split_plan(a, L, num_sms);
+  if (e != cudaSuccess) return e;
+  p.slots = reinterpret_cast<float*>(ws + L.off_slots);
+  p.items = reinterpret_cast<const int4*>(ws + L.off_items1);
+  p.item_count = reinterpret_cast<const int*>(ws);
+  prefill_kernel<<<dim3(static_cast<unsigned>(L.max1), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
+                   a.stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_split_scan(a, L)) != cudaSuccess) return e;
+  p.items = reinterpret_cast<const int4*>(ws + L.off_items3);
+  p.item_count = reinterpret_cast<const int*>(ws) + 1;
+  prefill_kernel<<<dim3(static_cast<unsigned>(L.max3), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
+                   a.stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -116,3 +116,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(kda, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(kda.KdaLibraryError):
         kda.library()
+
+
+def test_workspace_sizes(lib):
+    # without a GPU the library assumes 152 SMs for the planner's bound
+    assert kda.prefill_workspace_size(1, 96, 8192) == 0
+    assert kda.prefill_workspace_size(1, 8, 1 << 20) > 0
+    assert kda.prefill_workspace_size(4, 2, 10000, n_segments=1) == 0
+    assert kda.prefill_workspace_size(4, 2, 10000, n_segments=3) > 0
+    assert kda.prefill_workspace_size(4, 2, 10000, n_segments=-1) == 0

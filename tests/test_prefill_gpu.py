@@ -190,3 +190,69 @@ def test_varlen_full_sampled():
     off = inp.ckpt_off.tolist()
     for s in range(inp.n_seq):
         assert torch.equal(ck[off[s + 1] - 1], S[s]) or (inp.cu_seqlens[s + 1] - inp.cu_seqlens[s]) % 512 != 0
+
+
+# ------------------------------------------------------------------ sequence split (P8)
+def _weak(inp, scale):
+    inp.g.mul_(scale)  # slow decay: the transition M of a segment stays far from zero
+    return inp
+
+
+@pytest.mark.parametrize("n_seg", [2, 3, 7])
+@pytest.mark.parametrize("T", [1000, 2909])
+def test_split_forced_segments(n_seg, T):
+    inp = _weak(inputs.make_prefill([T], H=2, seed=200 + T + n_seg, device="cpu", decay="uniform", s0_std=0.02,
+                                    ckpt_every=64), 0.004)
+    o, S, ck, st, _ = run_gpu(inp, n_segments=n_seg)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
+
+
+def test_split_equals_unsplit_within_tolerance():
+    inp = _weak(inputs.make_prefill([4096], H=3, seed=301, device="cpu", decay="uniform", s0_std=0.02), 0.002)
+    o1, S1, _, st1, _ = run_gpu(inp, n_segments=1)
+    o4, S4, _, st4, _ = run_gpu(inp, n_segments=4)
+    assert st1 == 0 and st4 == 0
+    from kda_gpu_util import rel_fro as rf, rel_max as rm
+    assert rf(host(S4), host(S1)) <= S_TOL
+    assert rm(host(o4), host(o1)) <= O_TOL
+    check_against_oracle(inp, o4, S4, None)
+
+
+def test_split_varlen_packed_equals_standalone():
+    lens = [0, 1, 64, 65, 700, 1300]
+    inp = _weak(inputs.make_prefill(lens, H=2, seed=302, device="cpu", decay="uniform", s0_std=0.02,
+                                    ckpt_every=64), 0.01)
+    o, S, ck, st, o_buf = run_gpu(inp, n_segments=5, o_pad=64)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
+    assert torch.isnan(o_buf[:64].float()).all() and torch.isnan(o_buf[-64:].float()).all()
+    cu, off, pos = inp.cu_seqlens.tolist(), inp.ckpt_off.tolist(), inp.ckpt_pos.tolist()
+    for s in range(inp.n_seq):
+        a, b = cu[s], cu[s + 1]
+        one = inputs.PrefillInputs(inp.q[a:b], inp.k[a:b], inp.v[a:b], inp.g[a:b], inp.beta[a:b],
+                                   inp.S0[s:s + 1], torch.tensor([0, b - a], dtype=torch.int32),
+                                   torch.tensor([0, off[s + 1] - off[s]], dtype=torch.int32),
+                                   torch.tensor(pos[off[s]:off[s + 1]], dtype=torch.int32))
+        o1, S1, ck1, st1, _ = run_gpu(one, n_segments=5)
+        assert st1 == 0
+        assert torch.equal(o1, o[a:b]) and torch.equal(S1[0], S[s])
+        if off[s + 1] > off[s]:
+            assert torch.equal(ck1, ck[off[s]:off[s + 1]])
+
+
+def test_split_workspace_too_small_is_rejected():
+    inp = inputs.make_prefill([3000], H=2, seed=303, device="cpu")
+    d = to_device(inp)
+    need = kda.prefill_workspace_size(1, 2, 3000, n_segments=3)
+    assert need > 0
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kda.KdaError) as e:
+        kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], n_segments=3, workspace=ws)
+    assert e.value.status == 4
+
+
+def test_auto_planner_splits_few_heads_only():
+    assert kda.prefill_workspace_size(1, 96, 8192) == 0
+    assert kda.prefill_workspace_size(64, 96, 540672) == 0
+    assert kda.prefill_workspace_size(1, 8, 1 << 20) > 0
