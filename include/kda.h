@@ -128,6 +128,38 @@ kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, 
                        float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
                        size_t workspace_bytes, int* dev_status, cudaStream_t stream);
 
+
+/*
+ * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
+ *
+ * This entry point has no counterpart on the pages; it exists for the library's users.
+ * Some callers have no way to provide the workspace kda_prefill may ask for: a plugin
+ * inside a serving framework that owns all device memory and passes the plugin only its
+ * input and output tensors, or a path where cudaMalloc (which can synchronise the device)
+ * is not allowed.  This variant takes that scratch from a fixed array inside the library
+ * (KDA_NOALLOC_SCRATCH_BYTES = 32 MiB of device memory, held on every GPU where the library
+ * is loaded until the process exits) and otherwise behaves exactly like kda_prefill, with
+ * the same arguments minus workspace / workspace_bytes.  It allocates nothing.
+ *
+ *  - A problem whose kda_prefill_workspace_size(...) exceeds KDA_NOALLOC_SCRATCH_BYTES is
+ *    rejected with KDA_ERR_WORKSPACE before anything is enqueued (the 1M-token, 8-head
+ *    prefill with the library's own split needs about 30 MB; split counts forced through
+ *    n_segments can need more).
+ *  - The first call on each device, made while that device is current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call before any stream
+ *    capture on the device.
+ *  - Every call shares the one array and it keeps the previous call's contents (no part of
+ *    it needs to start at zero: each call writes every entry it reads).  Calls whose work
+ *    may overlap on the GPU -- on different streams, or from several host threads without
+ *    ordering -- race on it: order them on one stream.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+kda_status kda_prefill_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                               const float* beta, const float* S_in, const int32_t* cu_seqlens, int n_seq,
+                               int64_t total_tokens, const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt,
+                               kda_bf16* o, float* S_out, float* ckpts, int H, int d, int n_segments,
+                               int* dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

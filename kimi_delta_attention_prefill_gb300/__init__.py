@@ -63,6 +63,9 @@ def library():
             lib.kda_prefill.restype = _c_int
             lib.kda_prefill.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                         [_c_int, _c_int, _c_int, _vp, _c_sz, _vp, _vp])
+            lib.kda_prefill_noalloc.restype = _c_int
+            lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
+                                                [_c_int, _c_int, _c_int, _vp, _vp])
             _lib = lib
     return _lib
 
@@ -176,4 +179,51 @@ def prefill(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt_pos=Non
                                _stream_handle(stream))
     if st != 0:
         raise KdaError(st, "kda_prefill")
+    return o, S_out, ckpts
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def prefill_noalloc(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt_pos=None, o=None, S_out=None,
+                    ckpts=None, n_segments=0, dev_status=None, stream=None):
+    """:func:`prefill` for callers that cannot allocate device memory (``kda_prefill_noalloc``).
+
+    The library takes its scratch from a fixed 32 MiB array of its own instead of a
+    caller-provided workspace; larger problems raise ``KdaError`` (KDA_ERR_WORKSPACE).
+    Output tensors are created here only when not given; pass them in to allocate nothing.
+    Calls share the array: do not let two of them overlap on the GPU.
+    """
+    T, H, d = q.shape
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape)
+    _need(beta, "beta", torch.float32, (T, H))
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seq = cu_seqlens.shape[0] - 1
+    if S_in is not None:
+        _need(S_in, "S_in", torch.float32, (n_seq, H, d, d))
+    n_ckpt = 0
+    if ckpt_off is not None:
+        _need(ckpt_off, "ckpt_off", torch.int32, (n_seq + 1,))
+        _need(ckpt_pos, "ckpt_pos", torch.int32)
+        n_ckpt = ckpt_pos.shape[0]
+        if ckpts is None:
+            ckpts = torch.empty((n_ckpt, H, d, d), dtype=torch.float32, device=q.device)
+        _need(ckpts, "ckpts", torch.float32, (n_ckpt, H, d, d))
+    if o is None:
+        o = torch.empty((T, H, d), dtype=torch.bfloat16, device=q.device)
+    _need(o, "o", torch.bfloat16, (T, H, d))
+    if S_out is None:
+        S_out = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=q.device)
+    _need(S_out, "S_out", torch.float32, (n_seq, H, d, d))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_in),
+                                       _ptr(cu_seqlens), n_seq, T, _ptr(ckpt_off), _ptr(ckpt_pos), n_ckpt, _ptr(o),
+                                       _ptr(S_out), _ptr(ckpts), H, d, int(n_segments), _ptr(dev_status),
+                                       _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_prefill_noalloc")
     return o, S_out, ckpts
