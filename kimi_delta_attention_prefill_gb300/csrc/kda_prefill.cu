@@ -18,17 +18,24 @@
 //     column side B_tb[s] = K[s] exp(G[b_tb] - G[s]),  s < 16 (tb + 1)
 //                 = K[s] exp(G[b_sb(s)] - G[s]) * exp(G[b_tb] - G[b_sb(s)])
 //                   (first factor in [1, e^75], second <= 1)
-// and row block tb reads its entries from the MMA with B_tb.  Every tile, diagonal ones
-// included, is the same dense bf16 GEMM; nothing overflows.
+// and row block tb reads its entries from the product with B_tb.  The four B_tb are
+// stacked into one 160-row operand, so one dense bf16 GEMM (M = 128, N = 160) forms
+// every tile, the diagonal ones included; nothing overflows.
 //
 // Precision.  L / M_qk use bf16 operands (the rebased factors need bf16's exponent
 // range).  Every other product uses fp16 operands (11-bit significand, all values
 // bounded by the normalised keys) with fp32 accumulation in TMEM; INV is formed in fp32
 // on the CUDA cores.  The state lives in TMEM in fp32 for the whole sequence.
 //
-// One CTA (256 threads) runs one (sequence, head) chain serially over its chunks.
-// Thread 0 issues TMA copies and tcgen05 MMAs; completion is tracked with mbarriers,
-// every wait is bounded and a timeout ends the CTA with KDA_ERR_TIMEOUT.
+// Execution.  One CTA of 384 threads per work item, in two warp groups:
+//   recurrent (warps 0-3): the serial chain of chunk n -- K_decay S and Q_decay S, X,
+//       U, the state update and O -- on tcgen05 with the state resident in TMEM;
+//   prep (warps 4-11): everything that does not depend on the state, for chunk n + 1 --
+//       loads, cumsum, decay factors, scaled operands, L / M_qk, INV -- so it overlaps
+//       the recurrence ("部署 Kimi K3 ..." 1.1: overlap the intra-chunk work with the
+//       inter-chunk state hand-off).
+// The groups hand operands over through shared memory guarded by mbarriers; every wait
+// is bounded and a timeout ends the CTA with KDA_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -44,61 +51,71 @@ namespace kda {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kRThreads = 128;  // recurrent group: warps 0-3 (TMEM lane quarters 0-3)
+constexpr int kPThreads = 256;  // prep group: warps 4-11
+constexpr uint32_t kBarR = 1, kBarP = 2;  // named barrier ids
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns.  S uses the 128-lane layout (lane = d_k row); P/U and O are M = 64
-// accumulators (row t at lane 32 (t / 16) + t % 16).  The four L/M_qk accumulators
-// overlap O: they are consumed before O is first written in a chunk.
-constexpr uint32_t kTS = 0, kTP = 128, kTO = 256, kTLM = 256;
+// TMEM columns (all 128-lane layouts: lane = row of D).
+//   TS  [0, 128)   the state S, fp32 (lane = d_k row)
+//   TR1 [128, 256) lanes 0-63: P = K_decay S, then U; lanes 64-127: Q_decay S, then O
+//   TLM [256, 416) lanes 0-63: M_qk rows, lanes 64-127: L rows, 160 columns (4 blocks)
+constexpr uint32_t kTS = 0, kTR1 = 128, kTLM = 256;
 __host__ __device__ constexpr uint32_t lm_col(int tb) { return tb == 0 ? 0u : tb == 1 ? 16u : tb == 2 ? 48u : 96u; }
 
-// Shared-memory map (bytes from a 1024-aligned base).
-constexpr uint32_t SM_Q = 0;             // q tile (bf16, 2 K-panels)  -> Q_decay (fp16)
-constexpr uint32_t SM_K = 16384;         // k tile                    -> K_decay (fp16)
-constexpr uint32_t SM_G = 32768;         // g tile (fp32 [64][128])   -> [QA; KA] (bf16, 2 K-panels x 128 rows)
-constexpr uint32_t SM_V = 65536;         // v tiles, two stages of 16 KiB
-constexpr uint32_t SM_B = 98304;         // B_tb (bf16), 40 KiB      -> W, Ptmp, M_qk, INVbeta
-constexpr uint32_t SM_KR = 139264;       // K_restore (fp16, [t][i], 2 M-panels)
-constexpr uint32_t SM_XU = 155648;       // X then U (fp16, [t][j], 2 N-panels)
-constexpr uint32_t SM_S = 172032;        // S (fp16, [i][j], 2 N-panels x 128 rows)
-constexpr uint32_t SM_MISC = 204800;
-// inside SM_B after the L/M_qk products are consumed
-constexpr uint32_t SM_WL = SM_B;                 // fp32 [64][68]: L (strictly lower, row-scaled by beta)
-constexpr uint32_t SM_WI = SM_B + 17408;         // fp32 [64][68]: INV, built block by block
-constexpr uint32_t SM_PT = SM_B + 34816;         // fp32 4 x [16][16] block scratch (ends at SM_B + 38912)
-constexpr uint32_t SM_INVB = SM_B;               // fp16 [64][64] K-major INV Diag(beta) (over L, once dead)
-constexpr uint32_t SM_MQK = SM_MISC;             // fp16 [64][64] K-major M_qk (over the cumsum scratch)
-__host__ __device__ constexpr uint32_t btb_off(int tb) { return tb == 0 ? 0u : tb == 1 ? 4096u : tb == 2 ? 12288u : 24576u; }
-// misc
-constexpr uint32_t SM_TOT = SM_MISC;             // fp32 [16][128] token-quad sums
-constexpr uint32_t SM_GB = SM_TOT + 8192;        // fp32 [4][128] G at block starts
-constexpr uint32_t SM_GL = SM_GB + 2048;         // fp32 [128]    G at the last token
-constexpr uint32_t SM_AT = SM_GL + 512;          // fp32 [4][128] exp(G[b_tb])
-constexpr uint32_t SM_RT = SM_AT + 2048;         // fp32 [4][128] exp(G_last - G[b_tb])
-constexpr uint32_t SM_F = SM_RT + 2048;          // fp32 [6][128] exp(G[b_tb] - G[b_sb])
-constexpr uint32_t SM_AL = SM_F + 3072;          // fp32 [128]    a_last
-constexpr uint32_t SM_BETA = SM_AL + 512;        // fp32 [64]
-constexpr uint32_t SM_BAR = SM_BETA + 256;       // mbarriers
-constexpr uint32_t SM_CTRL = SM_BAR + 64;        // tmem slot, flags
+// Shared memory (bytes from a 1024-aligned base).
+constexpr uint32_t SM_S16 = 0;        // S fp16, [i][j], 2 N-panels x 128 rows        (recurrent)
+constexpr uint32_t SM_KQ = 32768;     // [K_decay; Q_decay] fp16, K-major, 2 x 128 rows (prep -> recurrent)
+constexpr uint32_t SM_V = 65536;      // v tiles (TMA), two stages of 16 KiB             (recurrent)
+constexpr uint32_t SM_XU = 98304;     // X, then U, fp16 [t][j], 2 N-panels x 64 rows    (recurrent)
+constexpr uint32_t SM_KR = 114688;    // K_restore fp16 [t][i], 2 M-panels x 64 rows     (prep -> recurrent)
+constexpr uint32_t SM_IM = 131072;    // [INV Diag(beta); M_qk] fp16, K-major, 128 rows  (prep -> recurrent)
+constexpr uint32_t SM_QAKA = 147456;  // [QA; KA] bf16, K-major, 2 x 128 rows            (prep)
+constexpr uint32_t SM_BT = 180224;    // B_0..B_3 bf16, K-major, 2 x 160 rows            (prep)
+constexpr uint32_t SM_MISC = 221184;
+constexpr uint32_t SM_WL = SM_BT;              // fp32 [64][68] L        (over B_tb, once consumed)
+constexpr uint32_t SM_WI = SM_BT + 17408;      // fp32 [64][68] INV
+constexpr uint32_t SM_PT = SM_BT + 34816;      // fp32 4 x [16][16] block scratch (ends at SM_BT + 38912)
+constexpr uint32_t SM_TOT = SM_MISC;           // fp32 [4][128] per-block sums of g (prep)
+constexpr uint32_t SM_AL = SM_TOT + 7168;      // fp32 [2][128] a_last by chunk parity (prep -> recurrent)
+constexpr uint32_t SM_BETA = SM_AL + 1024;     // fp32 [64]
+constexpr uint32_t SM_BAR = SM_BETA + 256;     // mbarriers
+constexpr uint32_t SM_CTRL = SM_BAR + 128;     // tmem base, flags
 constexpr uint32_t kSmemBytes = SM_CTRL + 64;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+static_assert(SM_BT + 40960 == SM_MISC, "layout");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
-enum { BAR_IN = 0, BAR_V0 = 1, BAR_V1 = 2, BAR_LM = 3, BAR_P = 4, BAR_U = 5, BAR_S = 6, kNumBars = 7 };
+enum {
+  BAR_V0 = 0, BAR_V1 = 1,  // v tile landed (TMA)
+  BAR_LM = 2,              // L / M_qk product done (prep's MMA)
+  BAR_M1 = 3,              // K_decay S, Q_decay S done
+  BAR_M2 = 4,              // U done
+  BAR_M34 = 5,             // state update and O done
+  BAR_KQ = 6,              // prep -> recurrent: [K_decay; Q_decay] and a_last of the chunk written
+  BAR_IM = 7,              // prep -> recurrent: [INV Diag(beta); M_qk] written
+  BAR_KR = 8,              // prep -> recurrent: K_restore written
+  BAR_QK = 9,              // raw q, k of the chunk landed in the [K_decay; Q_decay] buffer (TMA)
+  kNumBars = 10
+};
+enum { CTRL_TMEM = 0, CTRL_ABORT = 1, CTRL_VALID = 2 };
 
 struct Work {
   int seq, h;
-  int64_t bos;       // first packed row of the sequence
-  int len;           // tokens in the sequence
-  int c0, c1;        // chunk range [c0, c1) of this CTA
-  const float* entry;  // entry state [128][128] or nullptr (zeros)
-  float* s_out;        // final state destination or nullptr
+  int64_t bos;           // first packed row of the sequence
+  int len;               // tokens in the sequence
+  int c0, c1;            // chunk range [c0, c1) of this CTA
+  const float* entry;    // entry state [128][128] or nullptr (zeros)
+  float* s_out;          // final state destination or nullptr
   int ck_begin, ck_end;  // checkpoint slots this CTA may write
 };
 
 struct KParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_g;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const float* g;
   const float* beta;
   const float* S_in;
   const int32_t* cu;
@@ -116,7 +133,6 @@ struct KParams {
   float* slots;           // split-path state slots [slot][H][3][128][128]
 };
 
-__device__ __forceinline__ float4 ld4(const uint8_t* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
@@ -161,8 +177,7 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
 // L is 64 x 64 strictly lower triangular, fp32 in shared memory with row stride kLdw.
 // Block forward substitution over 16 x 16 blocks (D_i = (I + L_ii)^-1):
 //     INV_ii = D_i,   INV_ij = -D_i (L_ij D_j + sum_{j<k<i} L_ik INV_kj)   (i > j)
-// evaluated in dependency stages, one warp per 16 x 16 block product.  The result is
-// scaled by beta along columns and stored as the fp16 K-major operand INV Diag(beta).
+// evaluated in dependency stages, one warp per 16 x 16 block product.
 constexpr int kLdw = 68;  // padded row stride (floats): conflict-free float4 row reads
 
 // acc += A * B for 16 x 16 blocks; lane owns row lane / 2, columns 8 (lane % 2) .. +7.
@@ -199,16 +214,17 @@ __device__ __forceinline__ void blk_copy(const float* S, int lds, float* D, int 
   blk_store(D, ldd, acc, lane, 1.f);
 }
 
-// All 256 threads call this (it synchronises the CTA).
-__device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const float* beta, uint8_t* invb, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
+// Called by the 256 prep threads (ptid 0..255); synchronises the prep group only.
+// On return WI holds INV except block (3, 0), which is in PT block 3.
+__device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int ptid) {
+  const int warp = ptid >> 5, lane = ptid & 31;
   auto L = [&](int i, int j) { return WL + 16 * i * kLdw + 16 * j; };
   auto I = [&](int i, int j) { return WI + 16 * i * kLdw + 16 * j; };
   auto P = [&](int k) { return PT + 256 * k; };
 
   // diagonal blocks: thread (b, c) solves column c of (I + L_bb) x = e_c
-  if (tid < 64) {
-    const int b = tid >> 4, c = tid & 15;
+  if (ptid < 64) {
+    const int b = ptid >> 4, c = ptid & 15;
     const float* Lb = L(b, b);
     float x[16];
 #pragma unroll
@@ -222,7 +238,7 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const f
 #pragma unroll
     for (int r = 0; r < 16; ++r) Db[r * kLdw + c] = x[r];
   }
-  __syncthreads();
+  named_bar_sync(kBarP, kPThreads);
   // T_ij = L_ij D_j (stored where INV_ij will go)
   if (warp < 6) {
     const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
@@ -231,7 +247,7 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const f
     blk_mac(L(i, j), kLdw, I(j, j), kLdw, acc, lane);
     blk_store(I(i, j), kLdw, acc, lane, 1.f);
   }
-  __syncthreads();
+  named_bar_sync(kBarP, kPThreads);
   // INV_{i,i-1} = -D_i T_{i,i-1} -> P(i-1)
   if (warp < 3) {
     const int i = warp + 1;
@@ -239,7 +255,7 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const f
     blk_mac(I(i, i), kLdw, I(i, i - 1), kLdw, acc, lane);
     blk_store(P(i - 1), 16, acc, lane, -1.f);
   }
-  __syncthreads();
+  named_bar_sync(kBarP, kPThreads);
   // R_20 = T_20 + L_21 INV_10, R_31 = T_31 + L_32 INV_21 (in place); first sub-diagonal into place
   if (warp < 2) {
     const int i = warp + 2, j = warp;
@@ -251,7 +267,7 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const f
     const int k = warp - 2;
     blk_copy(P(k), 16, I(k + 1, k), kLdw, lane);
   }
-  __syncthreads();
+  named_bar_sync(kBarP, kPThreads);
   // INV_20 = -D_2 R_20 -> P(0), INV_31 = -D_3 R_31 -> P(1)
   if (warp < 2) {
     const int i = warp + 2, j = warp;
@@ -259,7 +275,7 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const f
     blk_mac(I(i, i), kLdw, I(i, j), kLdw, acc, lane);
     blk_store(P(j), 16, acc, lane, -1.f);
   }
-  __syncthreads();
+  named_bar_sync(kBarP, kPThreads);
   // R_30 = T_30 + L_31 INV_10 + L_32 INV_20 (in place); second sub-diagonal into place
   if (warp == 0) {
     float acc[8];
@@ -272,56 +288,526 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, const f
   } else if (warp == 2) {
     blk_copy(P(1), 16, I(3, 1), kLdw, lane);
   }
-  __syncthreads();
-  // INV_30 = -D_3 R_30 (warp 0, registers); every block -> INV Diag(beta), fp16, K-major [t][s].
-  // The fp16 operand overwrites L, which is no longer read.
-  auto put8 = [&](int t, int g, const float (&v)[8]) {
-    const int s0 = 8 * g;
-    st4(invb + sw128(t, 2 * s0), pack_half2(v[0] * beta[s0], v[1] * beta[s0 + 1]),
-        pack_half2(v[2] * beta[s0 + 2], v[3] * beta[s0 + 3]), pack_half2(v[4] * beta[s0 + 4], v[5] * beta[s0 + 5]),
-        pack_half2(v[6] * beta[s0 + 6], v[7] * beta[s0 + 7]));
-  };
+  named_bar_sync(kBarP, kPThreads);
+  // INV_30 = -D_3 R_30 -> P(3)
   if (warp == 0) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     blk_mac(I(3, 3), kLdw, I(3, 0), kLdw, acc, lane);
+    blk_store(P(3), 16, acc, lane, -1.f);
+  }
+  named_bar_sync(kBarP, kPThreads);
+}
+
+// INV Diag(beta) -> fp16 K-major rows 0..63 of the [INV Diag(beta); M_qk] operand.
+__device__ void put_inv_beta(const float* WI, const float* PT, const float* beta, uint8_t* dst, int ptid) {
+  for (int task = ptid; task < 512; task += kPThreads) {
+    const int t = task >> 3, g = task & 7, s0 = 8 * g;
+    float v[8];
+    if ((g >> 1) > (t >> 4)) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = -acc[e];
-    put8(48 + (lane >> 1), lane & 1, acc);
-  } else {
-    for (int task = tid - 32; task < 512; task += kThreads - 32) {
-      const int t = task >> 3, g = task & 7;
-      if (t >= 48 && g < 2) continue;  // block (3, 0): warp 0
-      float v[8];
-      if ((g >> 1) > (t >> 4)) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = 0.f;
-      } else {
-        const float4 x = *reinterpret_cast<const float4*>(WI + t * kLdw + 8 * g);
-        const float4 y = *reinterpret_cast<const float4*>(WI + t * kLdw + 8 * g + 4);
-        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-      }
-      put8(t, g, v);
+      for (int e = 0; e < 8; ++e) v[e] = 0.f;
+    } else {
+      const float* src = (t >= 48 && g < 2) ? PT + 3 * 256 + (t - 48) * 16 + s0 : WI + t * kLdw + s0;
+      const float4 x = *reinterpret_cast<const float4*>(src);
+      const float4 y = *reinterpret_cast<const float4*>(src + 4);
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
     }
+    st4(dst + sw128(t, 2 * s0), pack_half2(v[0] * beta[s0], v[1] * beta[s0 + 1]),
+        pack_half2(v[2] * beta[s0 + 2], v[3] * beta[s0 + 3]), pack_half2(v[4] * beta[s0 + 4], v[5] * beta[s0 + 5]),
+        pack_half2(v[6] * beta[s0 + 6], v[7] * beta[s0 + 7]));
   }
 }
 
-__device__ __forceinline__ void issue_tile_loads(const KParams& p, uint8_t* sm, uint64_t* bars, int which, int h,
-                                                 int64_t row0, int vstage) {
-  // which: bit0 q, bit1 k, bit2 g, bit3 v
-  const int r = static_cast<int>(row0);
-  if (which & 1) {
-    tma_load_3d(sm + SM_Q, &p.tm_q, &bars[BAR_IN], 0, h, r);
-    tma_load_3d(sm + SM_Q + 8192, &p.tm_q, &bars[BAR_IN], 64, h, r);
+// Raw q, k of a chunk (bf16, 128-byte swizzle) into the [K_decay; Q_decay] buffer: k to
+// rows 0..63, q to rows 64..127 of each 64-channel panel.
+__device__ __forceinline__ void issue_qk(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, int cidx) {
+  const int r0 = static_cast<int>(w.bos + static_cast<int64_t>(cidx) * kChunk);
+  mbar_arrive_expect_tx(&bars[BAR_QK], 32768);
+  tma_load_3d(sm + SM_KQ, &p.tm_k, &bars[BAR_QK], 0, w.h, r0);
+  tma_load_3d(sm + SM_KQ + 16384, &p.tm_k, &bars[BAR_QK], 64, w.h, r0);
+  tma_load_3d(sm + SM_KQ + 8192, &p.tm_q, &bars[BAR_QK], 0, w.h, r0);
+  tma_load_3d(sm + SM_KQ + 16384 + 8192, &p.tm_q, &bars[BAR_QK], 64, w.h, r0);
+}
+
+// ------------------------------------------------------------------ prep group
+// 256 threads.  Warp pw owns the 16-token block tb = pw / 2 and the 64-channel half
+// pw % 2; lane = 8 x (token quad in the block) + (channel group of 8).  Each 8-lane group
+// therefore writes one 128-byte row of every swizzled tile (conflict-free), and the block
+// index is uniform across the warp.
+//
+// The per-block decay reference is the cumulative log-decay just before the block,
+// Gx[tb] = G[16 tb - 1] (0 for tb = 0): the row side e^{G[t] - Gx[tb(t)]} is <= 1 and the
+// column side e^{Gx[tb] - G[s]} is <= e^{16 x 5} = e^80 for s in the block (the pages'
+// 16-token bound), <= 1 for earlier s.
+__device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
+                           uint32_t tmem, int n_chunks, int ptid) {
+  // Registers: the launch gives every thread 168; the recurrent group gives some back
+  // (128 x 112) so the prep group can hold its operand tiles (256 x 184); 61,440 of the
+  // block's 64,512 registers in total.
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
+  const int pw = ptid >> 5, lane = ptid & 31;
+  const int tb = pw >> 1, tql = lane >> 3;
+  const int cg = 8 * (pw & 1) + (lane & 7);  // channel group: channels 8 cg .. +7
+  const int kpanel = cg >> 3, kchunk = cg & 7;
+  const int t0 = 16 * tb + 4 * tql;          // first of this thread's 4 tokens
+  const int H = p.H, h = w.h;
+  const uint32_t tl = static_cast<uint32_t>((pw & 3) * 32) << 16;
+  float* s_beta = reinterpret_cast<float*>(sm + SM_BETA);
+  float* tot = reinterpret_cast<float*>(sm + SM_TOT);  // [4][128] per-block sums of g
+  const uint64_t dQAKA = smem_desc(smem_u32(sm + SM_QAKA), 16, 1024, kSwizzle128B);
+  const uint64_t dBT = smem_desc(smem_u32(sm + SM_BT), 16, 1024, kSwizzle128B);
+  const uint32_t id_lm = idesc_f16(128, 160, true, false, false);
+
+  // this thread's slice of a chunk's g (loaded one chunk ahead) and beta
+  float4 gx[4][2];
+  float beta_next = 0.f;
+  auto load_g = [&](int cidx, int u0, int u1) {
+    const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
+    const int valid = min(kChunk, w.len - cidx * kChunk);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (u < u0 || u >= u1) continue;
+      const int t = t0 + u;
+      if (t < valid) {
+        const float* src = p.g + ((row0 + t) * H + h) * kHeadDim + cg * 8;
+        gx[u][0] = *reinterpret_cast<const float4*>(src);
+        gx[u][1] = *reinterpret_cast<const float4*>(src + 4);
+      } else {
+        gx[u][0] = gx[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+  auto load_beta = [&](int cidx) {
+    const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
+    const int valid = min(kChunk, w.len - cidx * kChunk);
+    beta_next = (ptid < valid) ? p.beta[(row0 + ptid) * H + h] : 0.f;
+  };
+  if (ptid == 0) issue_qk(p, w, sm, bars, w.c0);
+  load_g(w.c0, 0, 4);
+  if (ptid < kChunk) load_beta(w.c0);
+
+  for (int n = 0; n < n_chunks; ++n) {
+    const int cidx = w.c0 + n;
+    const bool has_next = (n + 1) < n_chunks;
+    if (ptid == 0 && has_next) {  // pull the next chunk's tiles toward L2
+      const int rn = static_cast<int>(w.bos + static_cast<int64_t>(cidx + 1) * kChunk);
+      tma_prefetch_3d(&p.tm_g, 0, h, rn);
+      tma_prefetch_3d(&p.tm_q, 0, h, rn); tma_prefetch_3d(&p.tm_q, 64, h, rn);
+      tma_prefetch_3d(&p.tm_k, 0, h, rn); tma_prefetch_3d(&p.tm_k, 64, h, rn);
+      tma_prefetch_3d(&p.tm_v, 0, h, rn); tma_prefetch_3d(&p.tm_v, 64, h, rn);
+    }
+    if (ptid < kChunk) s_beta[ptid] = beta_next;
+
+    // ---- 1. cumsum of g: thread prefix over its 4 tokens, warp scan over the block's
+    //         4 quads, block sums exchanged through shared memory
+    float G[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      G[u][0] = gx[u][0].x; G[u][1] = gx[u][0].y; G[u][2] = gx[u][0].z; G[u][3] = gx[u][0].w;
+      G[u][4] = gx[u][1].x; G[u][5] = gx[u][1].y; G[u][6] = gx[u][1].z; G[u][7] = gx[u][1].w;
+    }
+    if (has_next) load_g(cidx + 1, 0, 2);
+    if (has_next && ptid < kChunk) load_beta(cidx + 1);
+#pragma unroll
+    for (int u = 1; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) G[u][e] += G[u - 1][e];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float run = G[3][e];
+      float y = __shfl_up_sync(0xffffffffu, run, 8);
+      if (tql >= 1) run += y;
+      y = __shfl_up_sync(0xffffffffu, run, 16);
+      if (tql >= 2) run += y;
+      const float excl = run - G[3][e];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) G[u][e] += excl;  // block-local inclusive cumsum
+      if (tql == 3) tot[tb * 128 + cg * 8 + e] = G[3][e];
+    }
+    named_bar_sync(kBarP, kPThreads);
+
+    // ---- 2. block references Gx[b] (sum of earlier blocks), G_last, decay factors.
+    //         G stays block-local: E = exp(G) = a / a(Gx[tb]) <= 1.
+    float atr[8], rtr[8], fr[3][8];
+    {
+      const int c = cg * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float s0 = tot[0 * 128 + c + e], s1 = tot[1 * 128 + c + e], s2 = tot[2 * 128 + c + e],
+                    s3 = tot[3 * 128 + c + e];
+        const float gx1 = s0, gx2 = s0 + s1, gx3 = s0 + s1 + s2, gl = gx3 + s3;
+        const float own = tb == 0 ? 0.f : tb == 1 ? gx1 : tb == 2 ? gx2 : gx3;
+        atr[e] = __expf(own);       // decay from the chunk start to the block reference
+        rtr[e] = __expf(gl - own);  // decay from the block reference to the chunk end
+        // F for the later row blocks b2 = tb + 1 .. 3: exp(Gx[b2] - Gx[tb]) <= 1
+        fr[0][e] = tb < 3 ? __expf((tb == 0 ? gx1 : tb == 1 ? gx2 : gx3) - own) : 0.f;
+        fr[1][e] = tb < 2 ? __expf((tb == 0 ? gx2 : gx3) - own) : 0.f;
+        fr[2][e] = tb < 1 ? __expf(gx3 - own) : 0.f;
+        if (tb == 0 && tql == 0) reinterpret_cast<float*>(sm + SM_AL)[(n & 1) * 128 + c + e] = __expf(gl);
+      }
+    }
+
+    // ---- 3. scaled operands.  Raw q, k sit in the [K_decay; Q_decay] buffer (TMA) and are
+    //         replaced in place (the recurrence released that buffer before the copy).
+    if (!mbar_wait(&bars[BAR_QK], n & 1)) ctrl[CTRL_ABORT] = 1;
+    const int valid = min(kChunk, w.len - cidx * kChunk);
+    uint32_t krq[4][4];
+    {
+      uint8_t* kqp = sm + SM_KQ + kpanel * 16384;
+      uint8_t* qap = sm + SM_QAKA + kpanel * 16384;
+      uint8_t* btp = sm + SM_BT + kpanel * 20480;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + u;
+        const uint32_t sk = sw128(t, 16 * kchunk), sq = sw128(64 + t, 16 * kchunk);
+        float qf[8], kf[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(kqp + sq), qf);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(kqp + sk), kf);
+        const bool m = t < valid;
+        float qa[8], ka[8], kb[8];
+        uint32_t qd2[4], kd2[4], qa2[4], ka2[4];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float kk = m ? kf[e] : 0.f;
+          const float E = __expf(G[u][e]);    // in [e^-80, 1]
+          const float Ei = __expf(-G[u][e]);  // in [1, e^80]
+          qa[e] = qf[e] * E;
+          ka[e] = kk * E;
+          kb[e] = kk * Ei;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qd2[e] = pack_half2(qa[2 * e] * atr[2 * e], qa[2 * e + 1] * atr[2 * e + 1]);
+          kd2[e] = pack_half2(ka[2 * e] * atr[2 * e], ka[2 * e + 1] * atr[2 * e + 1]);
+          krq[u][e] = pack_half2(kb[2 * e] * rtr[2 * e], kb[2 * e + 1] * rtr[2 * e + 1]);
+          qa2[e] = pack_bf162(qa[2 * e], qa[2 * e + 1]);
+          ka2[e] = pack_bf162(ka[2 * e], ka[2 * e + 1]);
+        }
+        st4(kqp + sk, kd2[0], kd2[1], kd2[2], kd2[3]);
+        st4(kqp + sq, qd2[0], qd2[1], qd2[2], qd2[3]);
+        st4(qap + sk, qa2[0], qa2[1], qa2[2], qa2[3]);
+        st4(qap + sq, ka2[0], ka2[1], ka2[2], ka2[3]);  // KA rows 64..127 share q's swizzle phase
+        // column-side operands: this block's rows of B_tb2 for every row block tb2 >= tb
+        st4(btp + sw128(lm_col(tb) + t, 16 * kchunk), pack_bf162(kb[0], kb[1]), pack_bf162(kb[2], kb[3]),
+            pack_bf162(kb[4], kb[5]), pack_bf162(kb[6], kb[7]));
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          if (tb + 1 + j > 3) break;
+          st4(btp + sw128(lm_col(tb + 1 + j) + t, 16 * kchunk),
+              pack_bf162(kb[0] * fr[j][0], kb[1] * fr[j][1]), pack_bf162(kb[2] * fr[j][2], kb[3] * fr[j][3]),
+              pack_bf162(kb[4] * fr[j][4], kb[5] * fr[j][5]), pack_bf162(kb[6] * fr[j][6], kb[7] * fr[j][7]));
+        }
+      }
+    }
+    if (has_next) load_g(cidx + 1, 2, 4);
+    fence_proxy_async_smem();
+    named_bar_sync(kBarP, kPThreads);
+    if (ptid == 0) {
+      mbar_arrive(&bars[BAR_KQ]);  // [K_decay; Q_decay] and a_last of this chunk are in place
+      tc_fence_after();            // L and M_qk: one M = 128, N = 160 product
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tmem + kTLM, dQAKA + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4),
+                dBT + (((kk >> 2) * 20480 + 32 * (kk & 3)) >> 4), id_lm, kk > 0);
+      mma_commit(&bars[BAR_LM]);
+    }
+
+    // ---- 4. L (fp32, beta-scaled) and M_qk (fp16, staged in the QA/KA region)
+    if (!mbar_wait(&bars[BAR_LM], n & 1)) ctrl[CTRL_ABORT] = 1;
+    tc_fence_after();
+    if (pw < 4) {
+      const int q = pw;  // TMEM lane quarter
+      const bool is_l = q >= 2;
+      const int t = (q & 1) * 32 + lane;
+      const int tbl = t >> 4;
+      const int g0 = (q & 1) ? 3 : 0, ng = (q & 1) ? 7 : 3;
+      const int lo = static_cast<int>(lm_col(tbl)), hi = lo + 16 * (tbl + 1);
+      const float bt = s_beta[t];
+      for (int gi = 0; gi < ng; ++gi) {
+        float r[16];
+        tmem_ld16(tmem + tl + kTLM + (g0 + gi) * 16, r);
+        tmem_wait_ld();
+        const int col = (g0 + gi) * 16;
+        if (col < lo || col >= hi) continue;
+        const int s0 = col - lo;
+        if (is_l) {
+          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + s0;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(wr + e) =
+                make_float4((s0 + e < t) ? bt * r[e] : 0.f, (s0 + e + 1 < t) ? bt * r[e + 1] : 0.f,
+                            (s0 + e + 2 < t) ? bt * r[e + 2] : 0.f, (s0 + e + 3 < t) ? bt * r[e + 3] : 0.f);
+        } else {
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = (s0 + e <= t) ? r[e] : 0.f;
+          uint8_t* mp = sm + SM_QAKA;
+          st4(mp + sw128(t, 2 * s0), pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
+              pack_half2(v[6], v[7]));
+          st4(mp + sw128(t, 2 * s0 + 16), pack_half2(v[8], v[9]), pack_half2(v[10], v[11]), pack_half2(v[12], v[13]),
+              pack_half2(v[14], v[15]));
+        }
+      }
+      for (int sb = tbl + 1; sb < 4; ++sb) {
+        if (is_l) {
+          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + sb * 16;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(wr + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          st4(sm + SM_QAKA + sw128(t, 32 * sb), 0, 0, 0, 0);
+          st4(sm + SM_QAKA + sw128(t, 32 * sb + 16), 0, 0, 0, 0);
+        }
+      }
+    }
+    named_bar_sync(kBarP, kPThreads);
+
+    // ---- 5. INV = (I + L)^-1
+    invert_unit_lower(reinterpret_cast<const float*>(sm + SM_WL), reinterpret_cast<float*>(sm + SM_WI),
+                      reinterpret_cast<float*>(sm + SM_PT), ptid);
+
+    // ---- 6. [INV Diag(beta); M_qk] and K_restore once the previous state update is done
+    if (n > 0 && !mbar_wait(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
+    put_inv_beta(reinterpret_cast<const float*>(sm + SM_WI), reinterpret_cast<const float*>(sm + SM_PT), s_beta,
+                 sm + SM_IM, ptid);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {  // M_qk rows: 8 KiB copied to rows 64..127 (same swizzle phase)
+      const int o = (ptid * 2 + c) * 16;
+      *reinterpret_cast<uint4*>(sm + SM_IM + 8192 + o) = *reinterpret_cast<const uint4*>(sm + SM_QAKA + o);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      st4(sm + SM_KR + kpanel * 8192 + sw128(t0 + u, 16 * kchunk), krq[u][0], krq[u][1], krq[u][2], krq[u][3]);
+    fence_proxy_async_smem();
+    named_bar_sync(kBarP, kPThreads);
+    if (ptid == 0) { mbar_arrive(&bars[BAR_IM]); mbar_arrive(&bars[BAR_KR]); }
+    if (ctrl[CTRL_ABORT]) break;
   }
-  if (which & 2) {
-    tma_load_3d(sm + SM_K, &p.tm_k, &bars[BAR_IN], 0, h, r);
-    tma_load_3d(sm + SM_K + 8192, &p.tm_k, &bars[BAR_IN], 64, h, r);
+}
+
+// ------------------------------------------------------------- recurrent group
+// 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (P, then U)
+// belong to warps 0-1, rows 64-127 (Q_decay S, then O) to warps 2-3; the state TS uses
+// all 128 lanes.
+__device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
+                                uint32_t tmem, int n_chunks, bool do_o, bool v_zero, bool entry_identity, int tid) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory");
+  const int rw = tid >> 5;
+  const uint32_t tl = static_cast<uint32_t>(rw * 32) << 16;
+  const uint64_t dS16 = smem_desc(smem_u32(sm + SM_S16), 16384, 1024, kSwizzle128B);
+  const uint64_t dKQ = smem_desc(smem_u32(sm + SM_KQ), 16, 1024, kSwizzle128B);
+  const uint64_t dXU = smem_desc(smem_u32(sm + SM_XU), 8192, 1024, kSwizzle128B);
+  const uint64_t dKR = smem_desc(smem_u32(sm + SM_KR), 8192, 1024, kSwizzle128B);
+  const uint64_t dIM = smem_desc(smem_u32(sm + SM_IM), 16, 1024, kSwizzle128B);
+  const uint32_t id_k_mn = idesc_f16(128, 128, false, false, true);
+  const uint32_t id_mn_mn = idesc_f16(128, 128, false, true, true);
+  const float* alast = reinterpret_cast<const float*>(sm + SM_AL);
+  const int i = tid;  // state row owned by this thread
+
+  // entry state -> TMEM (fp32) and the fp16 operand copy
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float r[32];
+    const int c0 = g * 32;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      float4 v4 = w.entry ? *reinterpret_cast<const float4*>(w.entry + i * kHeadDim + c0 + e) : make_float4(0, 0, 0, 0);
+      if (entry_identity)
+        v4 = make_float4(i == c0 + e ? 1.f : 0.f, i == c0 + e + 1 ? 1.f : 0.f, i == c0 + e + 2 ? 1.f : 0.f,
+                         i == c0 + e + 3 ? 1.f : 0.f);
+      r[e] = v4.x; r[e + 1] = v4.y; r[e + 2] = v4.z; r[e + 3] = v4.w;
+    }
+    tmem_st32(tmem + tl + kTS + c0, r);
+    uint8_t* dst = sm + SM_S16 + (g >> 1) * 16384;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      st4(dst + sw128(i, 64 * (g & 1) + 16 * c), pack_half2(r[8 * c], r[8 * c + 1]), pack_half2(r[8 * c + 2], r[8 * c + 3]),
+          pack_half2(r[8 * c + 4], r[8 * c + 5]), pack_half2(r[8 * c + 6], r[8 * c + 7]));
   }
-  if (which & 4) tma_load_3d(sm + SM_G, &p.tm_g, &bars[BAR_IN], 0, h, r);
-  if (which & 8) {
-    uint8_t* dst = sm + SM_V + vstage * 16384;
-    tma_load_3d(dst, &p.tm_v, &bars[BAR_V0 + vstage], 0, h, r);
-    tma_load_3d(dst + 8192, &p.tm_v, &bars[BAR_V0 + vstage], 64, h, r);
+  tmem_wait_st();
+  if (tid == 0) {
+    for (int s = 0; s < 2 && s < n_chunks; ++s) {
+      mbar_arrive_expect_tx(&bars[BAR_V0 + s], 16384);
+      const int r0 = static_cast<int>(w.bos + static_cast<int64_t>(w.c0 + s) * kChunk);
+      tma_load_3d(sm + SM_V + s * 16384, &p.tm_v, &bars[BAR_V0 + s], 0, w.h, r0);
+      tma_load_3d(sm + SM_V + s * 16384 + 8192, &p.tm_v, &bars[BAR_V0 + s], 64, w.h, r0);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  named_bar_sync(kBarR, kRThreads);
+
+  int ck = w.ck_begin;
+  for (int n = 0; n < n_chunks; ++n) {
+    const int cidx = w.c0 + n;
+    const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
+    const int valid = min(kChunk, w.len - cidx * kChunk);
+    const int vs = n & 1;
+    if (tid == 0 && n >= 1 && n + 1 < n_chunks) {  // stage vs ^ 1 was consumed by the previous chunk's X
+      mbar_arrive_expect_tx(&bars[BAR_V0 + (vs ^ 1)], 16384);
+      const int r0 = static_cast<int>(row0 + kChunk);
+      tma_load_3d(sm + SM_V + (vs ^ 1) * 16384, &p.tm_v, &bars[BAR_V0 + (vs ^ 1)], 0, w.h, r0);
+      tma_load_3d(sm + SM_V + (vs ^ 1) * 16384 + 8192, &p.tm_v, &bars[BAR_V0 + (vs ^ 1)], 64, w.h, r0);
+    }
+
+    // ---- P = K_decay S, Q_decay S (one M = 128 product)
+    if (!mbar_wait(&bars[BAR_KQ], n & 1)) ctrl[CTRL_ABORT] = 1;
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tmem + kTR1, dKQ + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4), dS16 + ((kk * 2048) >> 4), id_k_mn,
+                kk > 0);
+      mma_commit(&bars[BAR_M1]);
+    }
+    // ---- S <- Diag(a_last) S in TMEM (the previous update has completed)
+    {
+      const float al = alast[(n & 1) * 128 + i];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTS + g * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] *= al;
+        tmem_st32(tmem + tl + kTS + g * 32, r);
+      }
+      tmem_wait_st();
+    }
+    // ---- X = V - P (rows past the sequence end are zero)
+    if (!mbar_wait(&bars[BAR_M1], n & 1) || !mbar_wait(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
+    tc_fence_after();
+    if (tid == 0 && n + 1 < n_chunks) issue_qk(p, w, sm, bars, cidx + 1);  // the buffer is free again
+    if (rw < 2) {
+      const int t = tid;
+      const bool mk = t < valid;
+      const uint8_t* vt = sm + SM_V + vs * 16384;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+        tmem_wait_ld();
+        const uint8_t* vp = vt + (g >> 1) * 8192;
+        uint8_t* xp = sm + SM_XU + (g >> 1) * 8192;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float vv[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vp + sw128(t, 64 * (g & 1) + 16 * c)), vv);
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = mk ? (v_zero ? 0.f : vv[e]) - r[8 * c + e] : 0.f;
+          st4(xp + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]),
+              pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(kBarR, kRThreads);
+
+    // ---- U = INV Diag(beta) X (lanes 64-127 keep Q_decay S)
+    if (tid == 0) {
+      if (!mbar_wait(&bars[BAR_IM], n & 1)) ctrl[CTRL_ABORT] = 1;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), dXU + ((kk * 2048) >> 4), id_k_mn, kk > 0, 0u, 0u,
+                       0xffffffffu, 0xffffffffu);
+      mma_commit(&bars[BAR_M2]);
+    }
+    if (!mbar_wait(&bars[BAR_M2], n & 1)) ctrl[CTRL_ABORT] = 1;
+    tc_fence_after();
+    if (rw < 2) {
+      const int t = tid;
+      const bool mk = t < valid;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+        tmem_wait_ld();
+        uint8_t* up = sm + SM_XU + (g >> 1) * 8192;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float* x = r + 8 * c;
+          st4(up + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(mk ? x[0] : 0.f, mk ? x[1] : 0.f),
+              pack_half2(mk ? x[2] : 0.f, mk ? x[3] : 0.f), pack_half2(mk ? x[4] : 0.f, mk ? x[5] : 0.f),
+              pack_half2(mk ? x[6] : 0.f, mk ? x[7] : 0.f));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(kBarR, kRThreads);
+
+    // ---- S += K_restore^T U ; O += M_qk U (lanes 0-63 untouched)
+    if (tid == 0) {
+      if (!mbar_wait(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ud = dXU + ((kk * 2048) >> 4);
+        mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_mn_mn, 1);
+        if (do_o)
+          mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), ud, id_k_mn, 1, 0xffffffffu, 0xffffffffu, 0u, 0u);
+      }
+      mma_commit(&bars[BAR_M34]);
+    }
+    if (!mbar_wait(&bars[BAR_M34], n & 1)) ctrl[CTRL_ABORT] = 1;
+    tc_fence_after();
+    // ---- outputs (rows in lanes 64-127)
+    if (do_o && rw >= 2) {
+      const int t = tid - 64;
+      const bool wr = t < valid;
+      __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+        tmem_wait_ld();
+        if (wr) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + g * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pack_bf162(r[8 * c], r[8 * c + 1]), pack_bf162(r[8 * c + 2], r[8 * c + 3]),
+                                pack_bf162(r[8 * c + 4], r[8 * c + 5]), pack_bf162(r[8 * c + 6], r[8 * c + 7]));
+        }
+      }
+    }
+    // ---- state -> fp16 operand of the next chunk; checkpoint / final state in fp32
+    {
+      const int pos = min((cidx + 1) * kChunk, w.len);
+      float* ckdst = nullptr;
+      if (ck < w.ck_end && p.ckpt_pos[ck] == pos) {
+        ckdst = p.ckpts + (static_cast<int64_t>(ck) * p.H + w.h) * (kHeadDim * kHeadDim);
+        ++ck;
+      }
+      float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTS + g * 32, r);
+        tmem_wait_ld();
+        uint8_t* dst = sm + SM_S16 + (g >> 1) * 16384;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st4(dst + sw128(i, 64 * (g & 1) + 16 * c), pack_half2(r[8 * c], r[8 * c + 1]),
+              pack_half2(r[8 * c + 2], r[8 * c + 3]), pack_half2(r[8 * c + 4], r[8 * c + 5]),
+              pack_half2(r[8 * c + 6], r[8 * c + 7]));
+        if (ckdst) {
+          float4* d4 = reinterpret_cast<float4*>(ckdst + i * kHeadDim + g * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        }
+        if (fin) {
+          float4* d4 = reinterpret_cast<float4*>(fin + i * kHeadDim + g * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(kBarR, kRThreads);
+    if (ctrl[CTRL_ABORT]) break;
   }
 }
 
@@ -329,11 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM_BAR);
-  volatile int* ctrl = reinterpret_cast<volatile int*>(sm + SM_CTRL);  // [0] tmem base, [1] abort, [2] valid
-  float* s_beta = reinterpret_cast<float*>(sm + SM_BETA);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, hcol = warp >> 2;
+  volatile int* ctrl = reinterpret_cast<volatile int*>(sm + SM_CTRL);
+  const int tid = threadIdx.x, warp = tid >> 5;
 
   // ---- work item: (sequence, head, chunk range, mode)
   int4 it;
@@ -350,11 +833,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (tid == 0) {
     int64_t bos; int len, cb, ce;
     const bool ok = check_sequence(p, w.seq, bos, len, cb, ce);
-    ctrl[2] = ok ? 1 : 0;
+    ctrl[CTRL_VALID] = ok ? 1 : 0;
     if (!ok) report_status(p.status, 7 /* KDA_ERR_DEVICE_CHECK */);
   }
   __syncthreads();
-  if (!ctrl[2]) return;
+  if (!ctrl[CTRL_VALID]) return;
   const bool do_o = mode == kModeFull || mode == kModeFirst || mode == kModeTail;
   const bool v_zero = mode == kModeTrans, entry_identity = mode == kModeTrans;
   {
@@ -391,503 +874,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     return;
   }
 
-  // ---- setup: barriers, TMEM, tensor-map prefetch, first loads
+  // ---- setup: barriers, TMEM
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], 1);
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q); tma_prefetch_desc(&p.tm_k); tma_prefetch_desc(&p.tm_v); tma_prefetch_desc(&p.tm_g);
-    ctrl[1] = 0;
+    ctrl[CTRL_ABORT] = 0;
   }
   if (warp == 0) { tmem_alloc(reinterpret_cast<uint32_t*>(sm + SM_CTRL), kTmemCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = static_cast<uint32_t>(ctrl[0]);
-  const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;  // this warp's lane base
-
-  if (tid == 0) {
-    const int64_t row0 = w.bos + static_cast<int64_t>(w.c0) * kChunk;
-    mbar_arrive_expect_tx(&bars[BAR_IN], 65536);
-    issue_tile_loads(p, sm, bars, 1 | 2 | 4, w.h, row0, 0);
-    mbar_arrive_expect_tx(&bars[BAR_V0], 16384);
-    issue_tile_loads(p, sm, bars, 8, w.h, row0, 0);
-  }
-
-  // ---- entry state -> TMEM (fp32) and the fp16 operand copy
-  {
-    const int i = quarter * 32 + lane;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      float r[16];
-      const int c = hcol * 64 + m * 16;
-#pragma unroll
-      for (int e = 0; e < 16; e += 4) {
-        float4 v4 = w.entry ? *reinterpret_cast<const float4*>(w.entry + i * kHeadDim + c + e) : make_float4(0, 0, 0, 0);
-        if (entry_identity)
-          v4 = make_float4(i == c + e ? 1.f : 0.f, i == c + e + 1 ? 1.f : 0.f, i == c + e + 2 ? 1.f : 0.f,
-                           i == c + e + 3 ? 1.f : 0.f);
-        r[e] = v4.x; r[e + 1] = v4.y; r[e + 2] = v4.z; r[e + 3] = v4.w;
-      }
-      tmem_st16(tmem + tl + kTS + c, r);
-      uint8_t* dst = sm + SM_S + hcol * 16384;
-      st4(dst + sw128(i, 32 * m), pack_half2(r[0], r[1]), pack_half2(r[2], r[3]), pack_half2(r[4], r[5]),
-          pack_half2(r[6], r[7]));
-      st4(dst + sw128(i, 32 * m + 16), pack_half2(r[8], r[9]), pack_half2(r[10], r[11]), pack_half2(r[12], r[13]),
-          pack_half2(r[14], r[15]));
-    }
-    tmem_wait_st();
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-
-  // Descriptor bases; per-k-step offsets are added in 16-byte units.
-  const uint64_t dG = smem_desc(smem_u32(sm + SM_G), 16, 1024, kSwizzle128B);     // [QA; KA], K-panel 16384 B
-  const uint64_t dK = smem_desc(smem_u32(sm + SM_K), 16, 1024, kSwizzle128B);     // K_decay, K-panel 8192 B
-  const uint64_t dQ = smem_desc(smem_u32(sm + SM_Q), 16, 1024, kSwizzle128B);     // Q_decay
-  const uint64_t dS = smem_desc(smem_u32(sm + SM_S), 16384, 1024, kSwizzle128B);  // S, MN-major, k-step 2048 B
-  const uint64_t dInv = smem_desc(smem_u32(sm + SM_INVB), 16, 1024, kSwizzle128B);
-  const uint64_t dXU = smem_desc(smem_u32(sm + SM_XU), 8192, 1024, kSwizzle128B);  // MN-major, k-step 2048 B
-  const uint64_t dKR = smem_desc(smem_u32(sm + SM_KR), 8192, 1024, kSwizzle128B);  // MN-major A, k-step 2048 B
-  const uint64_t dMq = smem_desc(smem_u32(sm + SM_MQK), 16, 1024, kSwizzle128B);
-  const uint64_t dB0 = smem_desc(smem_u32(sm + SM_B), 16, 1024, kSwizzle128B);
-
-  int ck = w.ck_begin;
-  bool aborted = false;
+  const uint32_t tmem = static_cast<uint32_t>(ctrl[CTRL_TMEM]);
   const int n_chunks = w.c1 - w.c0;
-  float beta_next = 0.f;
-  if (tid < kChunk) {
-    const int64_t r = w.bos + static_cast<int64_t>(w.c0) * kChunk + tid;
-    beta_next = (tid < min(kChunk, w.len - w.c0 * kChunk)) ? p.beta[r * p.H + w.h] : 0.f;
-  }
-  for (int n = 0; n < n_chunks && !aborted; ++n) {
-    const int cidx = w.c0 + n;
-    const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
-    const int valid = min(kChunk, w.len - cidx * kChunk);
-    const int vstage = n & 1;
-    const bool has_next = (n + 1) < n_chunks;
-    const int64_t row_next = row0 + kChunk;
 
-    // ---- 1. inputs of this chunk
-    if (tid < kChunk) {
-      s_beta[tid] = beta_next;
-      const int vn = has_next ? min(kChunk, w.len - (cidx + 1) * kChunk) : 0;
-      beta_next = tid < vn ? p.beta[(row_next + tid) * p.H + w.h] : 0.f;
-    }
-    bool ok = mbar_wait(&bars[BAR_IN], n & 1) && mbar_wait(&bars[BAR_V0 + vstage], (n >> 1) & 1);
-    if (!ok) { if (tid == 0) ctrl[1] = 1; }
-    if (tid == 0 && ok && has_next) {
-      mbar_arrive_expect_tx(&bars[BAR_V0 + (vstage ^ 1)], 16384);
-      issue_tile_loads(p, sm, bars, 8, w.h, row_next, vstage ^ 1);
-    }
+  if (tid < kRThreads)
+    recurrent_group(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
+  else
+    prep_group(p, w, sm, bars, ctrl, tmem, n_chunks, tid - kRThreads);
 
-    // ---- 2. decay prep: cumsum, per-block factors, operands
-    const int tq = tid >> 4, cg = tid & 15, tb = tq >> 2;
-    float G[4][8];
-    {
-      const uint8_t* gt = sm + SM_G;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = tq * 4 + u;
-        float4 a = ld4(gt + t * 512 + cg * 32), b = ld4(gt + t * 512 + cg * 32 + 16);
-        const bool m = t < valid;
-        G[u][0] = m ? a.x : 0.f; G[u][1] = m ? a.y : 0.f; G[u][2] = m ? a.z : 0.f; G[u][3] = m ? a.w : 0.f;
-        G[u][4] = m ? b.x : 0.f; G[u][5] = m ? b.y : 0.f; G[u][6] = m ? b.z : 0.f; G[u][7] = m ? b.w : 0.f;
-      }
-#pragma unroll
-      for (int u = 1; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) G[u][e] += G[u - 1][e];
-      float* tot = reinterpret_cast<float*>(sm + SM_TOT);
-      *reinterpret_cast<float4*>(tot + tq * 128 + cg * 8) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
-      *reinterpret_cast<float4*>(tot + tq * 128 + cg * 8 + 4) = make_float4(G[3][4], G[3][5], G[3][6], G[3][7]);
-    }
-    __syncthreads();
-    if (ctrl[1]) { aborted = true; break; }
-    {
-      const float* tot = reinterpret_cast<const float*>(sm + SM_TOT);
-      float off[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int j = 0; j < tq; ++j) {
-        const float4 a = *reinterpret_cast<const float4*>(tot + j * 128 + cg * 8);
-        const float4 b = *reinterpret_cast<const float4*>(tot + j * 128 + cg * 8 + 4);
-        off[0] += a.x; off[1] += a.y; off[2] += a.z; off[3] += a.w;
-        off[4] += b.x; off[5] += b.y; off[6] += b.z; off[7] += b.w;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) G[u][e] += off[e];
-      if ((tq & 3) == 0) {
-        float* gb = reinterpret_cast<float*>(sm + SM_GB) + (tq >> 2) * 128 + cg * 8;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) gb[e] = G[0][e];
-      }
-      if (tq == 15) {
-        float* gl = reinterpret_cast<float*>(sm + SM_GL) + cg * 8;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) gl[e] = G[3][e];
-      }
-    }
-    __syncthreads();
-    {
-      const int i = tid & 127;
-      const float* gb = reinterpret_cast<const float*>(sm + SM_GB);
-      const float gl = reinterpret_cast<const float*>(sm + SM_GL)[i];
-      if (tid < 128) {
-        float* at = reinterpret_cast<float*>(sm + SM_AT);
-        float* rt = reinterpret_cast<float*>(sm + SM_RT);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          at[b * 128 + i] = __expf(gb[b * 128 + i]);
-          rt[b * 128 + i] = __expf(gl - gb[b * 128 + i]);
-        }
-        reinterpret_cast<float*>(sm + SM_AL)[i] = __expf(gl);
-      } else {
-        float* f = reinterpret_cast<float*>(sm + SM_F);
-        int idx = 0;
-#pragma unroll
-        for (int b = 1; b < 4; ++b)
-#pragma unroll
-          for (int s = 0; s < b; ++s, ++idx) f[idx * 128 + i] = __expf(gb[b * 128 + i] - gb[s * 128 + i]);
-      }
-    }
-    __syncthreads();
-    {
-      const float* gb = reinterpret_cast<const float*>(sm + SM_GB) + tb * 128 + cg * 8;
-      const float* at = reinterpret_cast<const float*>(sm + SM_AT) + tb * 128 + cg * 8;
-      const float* rt = reinterpret_cast<const float*>(sm + SM_RT) + tb * 128 + cg * 8;
-      const float* fp = reinterpret_cast<const float*>(sm + SM_F);
-      const int kpanel = cg >> 3, kchunk = cg & 7;
-      float gbr[8], atr[8], rtr[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) { gbr[e] = gb[e]; atr[e] = at[e]; rtr[e] = rt[e]; }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = tq * 4 + u;
-        const bool m = t < valid;
-        const uint32_t so = sw128(t, 16 * kchunk);
-        uint8_t* qp = sm + SM_Q + kpanel * 8192 + so;
-        uint8_t* kp = sm + SM_K + kpanel * 8192 + so;
-        float qf[8], kf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(qp), qf);
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(kp), kf);
-        float qd[8], kd[8], qa[8], ka[8], kb[8], kr[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float kk = m ? kf[e] : 0.f;
-          const float x = G[u][e] - gbr[e];   // <= 0, >= -75
-          const float E = __expf(x);
-          const float Ei = __expf(-x);
-          qa[e] = qf[e] * E;
-          ka[e] = kk * E;
-          qd[e] = qa[e] * atr[e];
-          kd[e] = ka[e] * atr[e];
-          kb[e] = kk * Ei;
-          kr[e] = kb[e] * rtr[e];
-        }
-        st4(qp, pack_half2(qd[0], qd[1]), pack_half2(qd[2], qd[3]), pack_half2(qd[4], qd[5]), pack_half2(qd[6], qd[7]));
-        st4(kp, pack_half2(kd[0], kd[1]), pack_half2(kd[2], kd[3]), pack_half2(kd[4], kd[5]), pack_half2(kd[6], kd[7]));
-        uint8_t* qa_p = sm + SM_G + kpanel * 16384;
-        st4(qa_p + so, pack_bf162(qa[0], qa[1]), pack_bf162(qa[2], qa[3]), pack_bf162(qa[4], qa[5]),
-            pack_bf162(qa[6], qa[7]));
-        st4(qa_p + sw128(64 + t, 16 * kchunk), pack_bf162(ka[0], ka[1]), pack_bf162(ka[2], ka[3]),
-            pack_bf162(ka[4], ka[5]), pack_bf162(ka[6], ka[7]));
-        st4(sm + SM_KR + kpanel * 8192 + so, pack_half2(kr[0], kr[1]), pack_half2(kr[2], kr[3]),
-            pack_half2(kr[4], kr[5]), pack_half2(kr[6], kr[7]));
-#pragma unroll
-        for (int tb2 = 0; tb2 < 4; ++tb2) {
-          if (tb2 < tb) continue;
-          float sc[8];
-          if (tb2 == tb) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sc[e] = kb[e];
-          } else {
-            const float* f = fp + ((tb2 * (tb2 - 1)) / 2 + tb) * 128 + cg * 8;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sc[e] = kb[e] * f[e];
-          }
-          const uint32_t rows = 16u * (tb2 + 1);
-          st4(sm + SM_B + btb_off(tb2) + kpanel * rows * 128 + so, pack_bf162(sc[0], sc[1]), pack_bf162(sc[2], sc[3]),
-              pack_bf162(sc[4], sc[5]), pack_bf162(sc[6], sc[7]));
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- 3. L / M_qk products (bf16) and K_decay S (fp16)
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t rows = 16u * (b + 1);
-        const uint32_t idesc = idesc_f16(128, rows, true, false, false);
-        const uint64_t db = dB0 + (btb_off(b) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = dG + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4);
-          const uint64_t bd = db + (((kk >> 2) * rows * 128 + 32 * (kk & 3)) >> 4);
-          mma_f16(tmem + kTLM + lm_col(b), ad, bd, idesc, kk > 0);
-        }
-      }
-      mma_commit(&bars[BAR_LM]);
-      const uint32_t idesc = idesc_f16(64, 128, false, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_f16(tmem + kTP, dK + (((kk >> 2) * 8192 + 32 * (kk & 3)) >> 4), dS + ((kk * 2048) >> 4), idesc, kk > 0);
-      mma_commit(&bars[BAR_P]);
-    }
-
-    // ---- 4. S <- Diag(a_last) S in TMEM (the previous chunk's update has completed)
-    {
-      const int i = quarter * 32 + lane;
-      const float al = reinterpret_cast<const float*>(sm + SM_AL)[i];
-      float r[4][16];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTS + hcol * 64 + m * 16, r[m]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) r[m][e] *= al;
-        tmem_st16(tmem + tl + kTS + hcol * 64 + m * 16, r[m]);
-      }
-      tmem_wait_st();
-    }
-
-    // ---- 5. read L and M_qk (row block tb reads the accumulator built with B_tb)
-    ok = mbar_wait(&bars[BAR_LM], n & 1);
-    if (!ok && tid == 0) ctrl[1] = 1;
-    tc_fence_after();
-    if (hcol == 0) {
-      // quarter 0/1: M_qk rows 0..63 ; quarter 2/3: L rows 0..63
-      const bool is_l = quarter >= 2;
-      const int t = (quarter & 1) * 32 + lane;
-      const int tbl = t >> 4;
-      const int g0 = (quarter & 1) ? 3 : 0, ng = (quarter & 1) ? 7 : 3;  // 16-column groups of this warp
-      const int lo = static_cast<int>(lm_col(tbl)), hi = lo + 16 * (tbl + 1);
-      const float bt = s_beta[t];
-      float r[7][16];
-#pragma unroll
-      for (int gi = 0; gi < 7; ++gi)
-        if (gi < ng) tmem_ld16(tmem + tl + kTLM + (g0 + gi) * 16, r[gi]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int gi = 0; gi < 7; ++gi) {
-        const int col = (g0 + gi) * 16;
-        if (gi >= ng || col < lo || col >= hi) continue;
-        const int s0 = col - lo;  // s block start
-        if (is_l) {
-          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + s0;
-#pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(wr + e) =
-                make_float4((s0 + e < t) ? bt * r[gi][e] : 0.f, (s0 + e + 1 < t) ? bt * r[gi][e + 1] : 0.f,
-                            (s0 + e + 2 < t) ? bt * r[gi][e + 2] : 0.f, (s0 + e + 3 < t) ? bt * r[gi][e + 3] : 0.f);
-        } else {
-          float v[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = (s0 + e <= t) ? r[gi][e] : 0.f;
-          uint8_t* mp = sm + SM_MQK;
-          st4(mp + sw128(t, 2 * s0), pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
-              pack_half2(v[6], v[7]));
-          st4(mp + sw128(t, 2 * s0 + 16), pack_half2(v[8], v[9]), pack_half2(v[10], v[11]), pack_half2(v[12], v[13]),
-              pack_half2(v[14], v[15]));
-        }
-      }
-      // zero the s blocks past this row's block
-      for (int sb = tbl + 1; sb < 4; ++sb) {
-        if (is_l) {
-          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + sb * 16;
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(wr + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          uint8_t* mp = sm + SM_MQK;
-          st4(mp + sw128(t, 32 * sb), 0, 0, 0, 0);
-          st4(mp + sw128(t, 32 * sb + 16), 0, 0, 0, 0);
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (ctrl[1]) { aborted = true; break; }
-
-    // ---- 6. next chunk's g; O = Q_decay S (fp16)
-    if (tid == 0) {
-      tc_fence_after();
-      if (has_next) {
-        mbar_arrive_expect_tx(&bars[BAR_IN], 65536);
-        issue_tile_loads(p, sm, bars, 4, w.h, row_next, 0);
-      }
-      if (do_o) {
-        const uint32_t idesc = idesc_f16(64, 128, false, false, true);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16(tmem + kTO, dQ + (((kk >> 2) * 8192 + 32 * (kk & 3)) >> 4), dS + ((kk * 2048) >> 4), idesc, kk > 0);
-      }
-    }
-
-    // ---- 7. INV = (I + L)^-1 in fp32 by 16 x 16 blocks, then INV Diag(beta) as fp16
-    invert_unit_lower(reinterpret_cast<float*>(sm + SM_WL), reinterpret_cast<float*>(sm + SM_WI),
-                      reinterpret_cast<float*>(sm + SM_PT), s_beta, sm + SM_INVB, tid);
-
-    // ---- 8. X = V - K_decay S  (rows past the sequence end are zero)
-    ok = mbar_wait(&bars[BAR_P], n & 1);
-    if (!ok && tid == 0) ctrl[1] = 1;
-    tc_fence_after();
-    {
-      const int t = quarter * 16 + (lane & 15);
-      const uint8_t* vt = sm + SM_V + vstage * 16384 + hcol * 8192;
-      uint8_t* xp = sm + SM_XU + hcol * 8192;
-      float r[4][16];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTP + hcol * 64 + m * 16, r[m]);
-      tmem_wait_ld();
-      if (lane < 16) {
-        const bool mk = t < valid;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float v0[8], v1[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vt + sw128(t, 32 * m)), v0);
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vt + sw128(t, 32 * m + 16)), v1);
-          float x[16];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            x[e] = mk ? (v_zero ? 0.f : v0[e]) - r[m][e] : 0.f;
-            x[8 + e] = mk ? (v_zero ? 0.f : v1[e]) - r[m][8 + e] : 0.f;
-          }
-          st4(xp + sw128(t, 32 * m), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
-              pack_half2(x[6], x[7]));
-          st4(xp + sw128(t, 32 * m + 16), pack_half2(x[8], x[9]), pack_half2(x[10], x[11]), pack_half2(x[12], x[13]),
-              pack_half2(x[14], x[15]));
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (ctrl[1]) { aborted = true; break; }
-
-    // ---- 9. next chunk's k; U = INV Diag(beta) X
-    if (tid == 0) {
-      tc_fence_after();
-      if (has_next) issue_tile_loads(p, sm, bars, 2, w.h, row_next, 0);
-      const uint32_t idesc = idesc_f16(64, 128, false, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) mma_f16(tmem + kTP, dInv + ((32 * kk) >> 4), dXU + ((kk * 2048) >> 4), idesc, kk > 0);
-      mma_commit(&bars[BAR_U]);
-    }
-
-    // ---- 10. U -> fp16 operand
-    ok = mbar_wait(&bars[BAR_U], n & 1);
-    if (!ok && tid == 0) ctrl[1] = 1;
-    tc_fence_after();
-    {
-      const int t = quarter * 16 + (lane & 15);
-      uint8_t* up = sm + SM_XU + hcol * 8192;
-      float r[4][16];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTP + hcol * 64 + m * 16, r[m]);
-      tmem_wait_ld();
-      if (lane < 16) {
-        const bool mk = t < valid;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[m][e] = mk ? r[m][e] : 0.f;
-          st4(up + sw128(t, 32 * m), pack_half2(r[m][0], r[m][1]), pack_half2(r[m][2], r[m][3]),
-              pack_half2(r[m][4], r[m][5]), pack_half2(r[m][6], r[m][7]));
-          st4(up + sw128(t, 32 * m + 16), pack_half2(r[m][8], r[m][9]), pack_half2(r[m][10], r[m][11]),
-              pack_half2(r[m][12], r[m][13]), pack_half2(r[m][14], r[m][15]));
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (ctrl[1]) { aborted = true; break; }
-
-    // ---- 11. next chunk's q; S += K_restore^T U; O += M_qk U
-    if (tid == 0) {
-      tc_fence_after();
-      if (has_next) issue_tile_loads(p, sm, bars, 1, w.h, row_next, 0);
-      const uint32_t id_s = idesc_f16(128, 128, false, true, true);
-      const uint32_t id_o = idesc_f16(64, 128, false, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ud = dXU + ((kk * 2048) >> 4);
-        mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_s, 1);
-        if (do_o) mma_f16(tmem + kTO, dMq + ((32 * kk) >> 4), ud, id_o, 1);
-      }
-      mma_commit(&bars[BAR_S]);
-    }
-
-    // ---- 12. outputs, next S operand, checkpoint / final state
-    ok = mbar_wait(&bars[BAR_S], n & 1);
-    if (!ok && tid == 0) ctrl[1] = 1;
-    tc_fence_after();
-    {
-      const int t = quarter * 16 + (lane & 15);
-      const bool wr = do_o && lane < 16 && t < valid;
-      __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim + hcol * 64;
-      float r[4][16];
-      if (do_o) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTO + hcol * 64 + m * 16, r[m]);
-        tmem_wait_ld();
-      }
-      if (wr) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + m * 16);
-          dst[0] = make_uint4(pack_bf162(r[m][0], r[m][1]), pack_bf162(r[m][2], r[m][3]), pack_bf162(r[m][4], r[m][5]),
-                              pack_bf162(r[m][6], r[m][7]));
-          dst[1] = make_uint4(pack_bf162(r[m][8], r[m][9]), pack_bf162(r[m][10], r[m][11]),
-                              pack_bf162(r[m][12], r[m][13]), pack_bf162(r[m][14], r[m][15]));
-        }
-      }
-    }
-    {
-      const int pos = min((cidx + 1) * kChunk, w.len);
-      float* ckdst = nullptr;
-      if (ck < w.ck_end && p.ckpt_pos[ck] == pos) {
-        ckdst = p.ckpts + (static_cast<int64_t>(ck) * p.H + w.h) * (kHeadDim * kHeadDim);
-        ++ck;
-      }
-      float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
-      const int i = quarter * 32 + lane;
-      uint8_t* dst = sm + SM_S + hcol * 16384;
-      float r[4][16];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) tmem_ld16(tmem + tl + kTS + hcol * 64 + m * 16, r[m]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int c = hcol * 64 + m * 16;
-        st4(dst + sw128(i, 32 * m), pack_half2(r[m][0], r[m][1]), pack_half2(r[m][2], r[m][3]),
-            pack_half2(r[m][4], r[m][5]), pack_half2(r[m][6], r[m][7]));
-        st4(dst + sw128(i, 32 * m + 16), pack_half2(r[m][8], r[m][9]), pack_half2(r[m][10], r[m][11]),
-            pack_half2(r[m][12], r[m][13]), pack_half2(r[m][14], r[m][15]));
-        if (ckdst) {
-          float4* d4 = reinterpret_cast<float4*>(ckdst + i * kHeadDim + c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_float4(r[m][4 * e], r[m][4 * e + 1], r[m][4 * e + 2], r[m][4 * e + 3]);
-        }
-        if (fin) {
-          float4* d4 = reinterpret_cast<float4*>(fin + i * kHeadDim + c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_float4(r[m][4 * e], r[m][4 * e + 1], r[m][4 * e + 2], r[m][4 * e + 3]);
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (ctrl[1]) { aborted = true; break; }
-  }
-
-  if (aborted) {
+  __syncthreads();
+  if (ctrl[CTRL_ABORT]) {
     // Let copies and MMAs still in flight land before TMEM is released (bounded).
     if (tid == 0) {
       report_status(p.status, 6 /* KDA_ERR_TIMEOUT */);
@@ -943,6 +950,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
         !make_map(&p.tm_v, a.v, false, a.H, T) || !make_map(&p.tm_g, a.g, true, a.H, T))
       return cudaErrorInvalidValue;
   }
+  p.q = static_cast<const __nv_bfloat16*>(a.q); p.k = static_cast<const __nv_bfloat16*>(a.k); p.g = a.g;
   p.beta = a.beta; p.S_in = a.S_in; p.cu = a.cu_seqlens; p.ckpt_off = a.ckpt_off; p.ckpt_pos = a.ckpt_pos;
   p.o = static_cast<__nv_bfloat16*>(a.o); p.S_out = a.S_out; p.ckpts = a.ckpts; p.status = a.status;
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
