@@ -76,7 +76,7 @@ constexpr uint32_t SM_BT = 180224;    // B_0..B_3 bf16, K-major, 2 x 160 rows   
 constexpr uint32_t SM_MISC = 221184;
 constexpr uint32_t SM_WL = SM_BT;              // fp32 [64][68] L        (over B_tb, once consumed)
 constexpr uint32_t SM_WI = SM_BT + 17408;      // fp32 [64][68] INV
-constexpr uint32_t SM_PT = SM_BT + 34816;      // fp32 4 x [16][16] block scratch (ends at SM_BT + 38912)
+constexpr uint32_t SM_PT = SM_BT + 34816;      // fp32 4 x [16][20] block scratch (ends at SM_BT + 39936)
 constexpr uint32_t SM_TOT = SM_MISC;           // fp32 [4][128] per-block sums of g (prep)
 constexpr uint32_t SM_AL = SM_TOT + 7168;      // fp32 [2][128] a_last by chunk parity (prep -> recurrent)
 constexpr uint32_t SM_BETA = SM_AL + 1024;     // fp32 [64]
@@ -97,7 +97,8 @@ enum {
   BAR_IM = 7,              // prep -> recurrent: [INV Diag(beta); M_qk] written
   BAR_KR = 8,              // prep -> recurrent: K_restore written
   BAR_QK = 9,              // raw q, k of the chunk landed in the [K_decay; Q_decay] buffer (TMA)
-  kNumBars = 10
+  BAR_G = 10,              // g of the chunk landed in the QA/KA region (TMA)
+  kNumBars = 11
 };
 enum { CTRL_TMEM = 0, CTRL_ABORT = 1, CTRL_VALID = 2 };
 
@@ -179,10 +180,17 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
 //     INV_ii = D_i,   INV_ij = -D_i (L_ij D_j + sum_{j<k<i} L_ik INV_kj)   (i > j)
 // evaluated in dependency stages, one warp per 16 x 16 block product.
 constexpr int kLdw = 68;  // padded row stride (floats): conflict-free float4 row reads
+constexpr int kLdp = 20;  // row stride of the 16 x 16 scratch blocks (conflict-free 8-row reads)
 
-// acc += A * B for 16 x 16 blocks; lane owns row lane / 2, columns 8 (lane % 2) .. +7.
-__device__ __forceinline__ void blk_mac(const float* A, int lda, const float* B, int ldb, float (&acc)[8], int lane) {
-  const int r = lane >> 1, c0 = (lane & 1) * 8;
+// Called by the 256 prep threads (ptid 0..255); synchronises the prep group only.
+// INV = (I + L)^-1 for L strictly lower (64 x 64, fp32, row stride kLdw in WL), by 16 x 16
+// blocks: with D = blockdiag((I + L_ii)^-1) and N = D L_off (strictly block-lower, N^4 = 0),
+//     (I + L) = blockdiag(I + L_ii) (I + N)  =>  INV = (I - N + N^2 - N^3) D.
+// On return WI holds INV (all blocks, upper blocks not written: the reader masks them).
+// `half`-warp products: a 16 x 16 x 16 product is split over two warps (8 rows each).
+__device__ __forceinline__ void blk_mac8(const float* A, int lda, const float* B, int ldb, float (&acc)[4], int lane,
+                                         int rbase) {
+  const int r = rbase + (lane >> 2), c0 = (lane & 3) * 4;
   float a[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -191,38 +199,26 @@ __device__ __forceinline__ void blk_mac(const float* A, int lda, const float* B,
   }
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    const float4 b0 = *reinterpret_cast<const float4*>(B + k * ldb + c0);
-    const float4 b1 = *reinterpret_cast<const float4*>(B + k * ldb + c0 + 4);
-    acc[0] += a[k] * b0.x; acc[1] += a[k] * b0.y; acc[2] += a[k] * b0.z; acc[3] += a[k] * b0.w;
-    acc[4] += a[k] * b1.x; acc[5] += a[k] * b1.y; acc[6] += a[k] * b1.z; acc[7] += a[k] * b1.w;
+    const float4 b = *reinterpret_cast<const float4*>(B + k * ldb + c0);
+    acc[0] += a[k] * b.x; acc[1] += a[k] * b.y; acc[2] += a[k] * b.z; acc[3] += a[k] * b.w;
   }
 }
-__device__ __forceinline__ void blk_load(const float* C, int ldc, float (&acc)[8], int lane) {
-  const int r = lane >> 1, c0 = (lane & 1) * 8;
-  const float4 x = *reinterpret_cast<const float4*>(C + r * ldc + c0);
-  const float4 y = *reinterpret_cast<const float4*>(C + r * ldc + c0 + 4);
-  acc[0] = x.x; acc[1] = x.y; acc[2] = x.z; acc[3] = x.w; acc[4] = y.x; acc[5] = y.y; acc[6] = y.z; acc[7] = y.w;
+__device__ __forceinline__ void blk_ld8(const float* C, int ldc, float (&acc)[4], int lane, int rbase, float sign) {
+  const float4 x = *reinterpret_cast<const float4*>(C + (rbase + (lane >> 2)) * ldc + (lane & 3) * 4);
+  acc[0] = sign * x.x; acc[1] = sign * x.y; acc[2] = sign * x.z; acc[3] = sign * x.w;
 }
-__device__ __forceinline__ void blk_store(float* C, int ldc, const float (&acc)[8], int lane, float sign) {
-  const int r = lane >> 1, c0 = (lane & 1) * 8;
-  *reinterpret_cast<float4*>(C + r * ldc + c0) = make_float4(sign * acc[0], sign * acc[1], sign * acc[2], sign * acc[3]);
-  *reinterpret_cast<float4*>(C + r * ldc + c0 + 4) = make_float4(sign * acc[4], sign * acc[5], sign * acc[6], sign * acc[7]);
-}
-__device__ __forceinline__ void blk_copy(const float* S, int lds, float* D, int ldd, int lane) {
-  float acc[8];
-  blk_load(S, lds, acc, lane);
-  blk_store(D, ldd, acc, lane, 1.f);
+__device__ __forceinline__ void blk_st8(float* C, int ldc, const float (&acc)[4], int lane, int rbase, float sign) {
+  *reinterpret_cast<float4*>(C + (rbase + (lane >> 2)) * ldc + (lane & 3) * 4) =
+      make_float4(sign * acc[0], sign * acc[1], sign * acc[2], sign * acc[3]);
 }
 
-// Called by the 256 prep threads (ptid 0..255); synchronises the prep group only.
-// On return WI holds INV except block (3, 0), which is in PT block 3.
 __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int ptid) {
   const int warp = ptid >> 5, lane = ptid & 31;
   auto L = [&](int i, int j) { return WL + 16 * i * kLdw + 16 * j; };
   auto I = [&](int i, int j) { return WI + 16 * i * kLdw + 16 * j; };
-  auto P = [&](int k) { return PT + 256 * k; };
+  auto P = [&](int k) { return PT + 320 * k; };  // 16 x 16 blocks, row stride kLdp
 
-  // diagonal blocks: thread (b, c) solves column c of (I + L_bb) x = e_c
+  // D_b: thread (b, c) solves column c of (I + L_bb) x = e_c  -> WI(b, b)
   if (ptid < 64) {
     const int b = ptid >> 4, c = ptid & 15;
     const float* Lb = L(b, b);
@@ -239,67 +235,97 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int pti
     for (int r = 0; r < 16; ++r) Db[r * kLdw + c] = x[r];
   }
   named_bar_sync(kBarP, kPThreads);
-  // T_ij = L_ij D_j (stored where INV_ij will go)
+  // N_ij = D_i L_ij for (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) -> WI(i, j); 6 products, 8 warps
+  // (warps 0-5 one product each; warps 6, 7 split (3,0) with... kept simple: one warp per product)
   if (warp < 6) {
     const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
     const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    blk_mac(L(i, j), kLdw, I(j, j), kLdw, acc, lane);
-    blk_store(I(i, j), kLdw, acc, lane, 1.f);
+    float a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
+    blk_mac8(I(i, i), kLdw, L(i, j), kLdw, a0, lane, 0);
+    blk_mac8(I(i, i), kLdw, L(i, j), kLdw, a1, lane, 8);
+    blk_st8(I(i, j), kLdw, a0, lane, 0, 1.f);
+    blk_st8(I(i, j), kLdw, a1, lane, 8, 1.f);
   }
   named_bar_sync(kBarP, kPThreads);
-  // INV_{i,i-1} = -D_i T_{i,i-1} -> P(i-1)
-  if (warp < 3) {
-    const int i = warp + 1;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    blk_mac(I(i, i), kLdw, I(i, i - 1), kLdw, acc, lane);
-    blk_store(P(i - 1), 16, acc, lane, -1.f);
+  // second-order terms (two warps per product, 8 rows each):
+  //   P0 = N_21 N_10, P1 = N_32 N_21, P2 = N_31 N_10 + N_32 N_20
+  {
+    const int prod = warp >> 1, rb = (warp & 1) * 8;
+    if (prod == 0) {
+      float a[4] = {0, 0, 0, 0};
+      blk_mac8(I(2, 1), kLdw, I(1, 0), kLdw, a, lane, rb);
+      blk_st8(P(0), kLdp, a, lane, rb, 1.f);
+    } else if (prod == 1) {
+      float a[4] = {0, 0, 0, 0};
+      blk_mac8(I(3, 2), kLdw, I(2, 1), kLdw, a, lane, rb);
+      blk_st8(P(1), kLdp, a, lane, rb, 1.f);
+    } else if (prod == 2) {
+      float a[4] = {0, 0, 0, 0};
+      blk_mac8(I(3, 1), kLdw, I(1, 0), kLdw, a, lane, rb);
+      blk_mac8(I(3, 2), kLdw, I(2, 0), kLdw, a, lane, rb);
+      blk_st8(P(2), kLdp, a, lane, rb, 1.f);
+    }
   }
   named_bar_sync(kBarP, kPThreads);
-  // R_20 = T_20 + L_21 INV_10, R_31 = T_31 + L_32 INV_21 (in place); first sub-diagonal into place
-  if (warp < 2) {
-    const int i = warp + 2, j = warp;
-    float acc[8];
-    blk_load(I(i, j), kLdw, acc, lane);
-    blk_mac(L(i, i - 1), kLdw, P(j), 16, acc, lane);
-    blk_store(I(i, j), kLdw, acc, lane, 1.f);
-  } else if (warp < 5) {
-    const int k = warp - 2;
-    blk_copy(P(k), 16, I(k + 1, k), kLdw, lane);
+  // M = -N + N^2 - N^3 (strictly block lower) into P(.) / WI:
+  //   M_10 = -N_10, M_21 = -N_21, M_32 = -N_32 (negated in the last stage)
+  //   M_20 = -N_20 + P0 -> P(0) ; M_31 = -N_31 + P1 -> P(1) ; M_30 = -N_30 + P2 - N_32 P0 -> P(2)
+  {
+    const int task = warp >> 1, rb = (warp & 1) * 8;
+    if (task == 0) {
+      float a[4];
+      blk_ld8(P(0), kLdp, a, lane, rb, 1.f);
+      float n[4];
+      blk_ld8(I(2, 0), kLdw, n, lane, rb, 1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] -= n[e];
+      blk_st8(P(3), kLdp, a, lane, rb, 1.f);  // M_20 (P(0) is still read by task 2)
+    } else if (task == 1) {
+      float a[4];
+      blk_ld8(P(1), kLdp, a, lane, rb, 1.f);
+      float n[4];
+      blk_ld8(I(3, 1), kLdw, n, lane, rb, 1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] -= n[e];
+      blk_st8(P(1), kLdp, a, lane, rb, 1.f);  // M_31 in place (own elements only)
+    } else if (task == 2) {
+      float a[4];
+      blk_ld8(P(2), kLdp, a, lane, rb, 1.f);
+      float n[4];
+      blk_ld8(I(3, 0), kLdw, n, lane, rb, 1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] -= n[e];
+      float c[4] = {0, 0, 0, 0};
+      blk_mac8(I(3, 2), kLdw, P(0), kLdp, c, lane, rb);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] -= c[e];
+      blk_st8(P(2), kLdp, a, lane, rb, 1.f);  // M_30 in place (own elements only)
+    }
   }
   named_bar_sync(kBarP, kPThreads);
-  // INV_20 = -D_2 R_20 -> P(0), INV_31 = -D_3 R_31 -> P(1)
-  if (warp < 2) {
-    const int i = warp + 2, j = warp;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    blk_mac(I(i, i), kLdw, I(i, j), kLdw, acc, lane);
-    blk_store(P(j), 16, acc, lane, -1.f);
-  }
-  named_bar_sync(kBarP, kPThreads);
-  // R_30 = T_30 + L_31 INV_10 + L_32 INV_20 (in place); second sub-diagonal into place
-  if (warp == 0) {
-    float acc[8];
-    blk_load(I(3, 0), kLdw, acc, lane);
-    blk_mac(L(3, 1), kLdw, I(1, 0), kLdw, acc, lane);
-    blk_mac(L(3, 2), kLdw, P(0), 16, acc, lane);
-    blk_store(I(3, 0), kLdw, acc, lane, 1.f);
-  } else if (warp == 1) {
-    blk_copy(P(0), 16, I(2, 0), kLdw, lane);
-  } else if (warp == 2) {
-    blk_copy(P(1), 16, I(3, 1), kLdw, lane);
-  }
-  named_bar_sync(kBarP, kPThreads);
-  // INV_30 = -D_3 R_30 -> P(3)
-  if (warp == 0) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    blk_mac(I(3, 3), kLdw, I(3, 0), kLdw, acc, lane);
-    blk_store(P(3), 16, acc, lane, -1.f);
+  // INV_ij = M_ij D_j: six products, warps 0-5 (16 rows each as two 8-row halves)
+  if (warp < 6) {
+    const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
+    const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
+    const float* M;
+    int ldm;
+    float sgn = 1.f;
+    if (i == j + 1) { M = I(i, j); ldm = kLdw; sgn = -1.f; }  // M = -N on the first sub-diagonal
+    else if (i == 2) { M = P(3); ldm = kLdp; }                   // (2,0)
+    else if (j == 1) { M = P(1); ldm = kLdp; }                   // (3,1)
+    else { M = P(2); ldm = kLdp; }                               // (3,0)
+    float a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
+    blk_mac8(M, ldm, I(j, j), kLdw, a0, lane, 0);
+    blk_mac8(M, ldm, I(j, j), kLdw, a1, lane, 8);
+    __syncwarp();  // every lane has read its rows of M (this warp's block only) before the store
+    blk_st8(I(i, j), kLdw, a0, lane, 0, sgn);
+    blk_st8(I(i, j), kLdw, a1, lane, 8, sgn);
   }
   named_bar_sync(kBarP, kPThreads);
 }
 
 // INV Diag(beta) -> fp16 K-major rows 0..63 of the [INV Diag(beta); M_qk] operand.
-__device__ void put_inv_beta(const float* WI, const float* PT, const float* beta, uint8_t* dst, int ptid) {
+__device__ void put_inv_beta(const float* WI, const float* beta, uint8_t* dst, int ptid) {
   for (int task = ptid; task < 512; task += kPThreads) {
     const int t = task >> 3, g = task & 7, s0 = 8 * g;
     float v[8];
@@ -307,7 +333,7 @@ __device__ void put_inv_beta(const float* WI, const float* PT, const float* beta
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = 0.f;
     } else {
-      const float* src = (t >= 48 && g < 2) ? PT + 3 * 256 + (t - 48) * 16 + s0 : WI + t * kLdw + s0;
+      const float* src = WI + t * kLdw + s0;
       const float4 x = *reinterpret_cast<const float4*>(src);
       const float4 y = *reinterpret_cast<const float4*>(src + 4);
       v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
@@ -342,9 +368,9 @@ __device__ __forceinline__ void issue_qk(const KParams& p, const Work& w, uint8_
 __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                            uint32_t tmem, int n_chunks, int ptid) {
   // Registers: the launch gives every thread 168; the recurrent group gives some back
-  // (128 x 112) so the prep group can hold its operand tiles (256 x 184); 61,440 of the
+  // (128 x 104) so the prep group can hold its operand tiles (256 x 192); 62,464 of the
   // block's 64,512 registers in total.
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
   const int pw = ptid >> 5, lane = ptid & 31;
   const int tb = pw >> 1, tql = lane >> 3;
   const int cg = 8 * (pw & 1) + (lane & 7);  // channel group: channels 8 cg .. +7
@@ -358,32 +384,19 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
   const uint64_t dBT = smem_desc(smem_u32(sm + SM_BT), 16, 1024, kSwizzle128B);
   const uint32_t id_lm = idesc_f16(128, 160, true, false, false);
 
-  // this thread's slice of a chunk's g (loaded one chunk ahead) and beta
-  float4 gx[4][2];
+  // beta of the next chunk (loaded one chunk ahead); g arrives by TMA in the QA/KA region
   float beta_next = 0.f;
-  auto load_g = [&](int cidx, int u0, int u1) {
-    const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
-    const int valid = min(kChunk, w.len - cidx * kChunk);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (u < u0 || u >= u1) continue;
-      const int t = t0 + u;
-      if (t < valid) {
-        const float* src = p.g + ((row0 + t) * H + h) * kHeadDim + cg * 8;
-        gx[u][0] = *reinterpret_cast<const float4*>(src);
-        gx[u][1] = *reinterpret_cast<const float4*>(src + 4);
-      } else {
-        gx[u][0] = gx[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
+  auto issue_g = [&](int cidx) {
+    const int r0 = static_cast<int>(w.bos + static_cast<int64_t>(cidx) * kChunk);
+    mbar_arrive_expect_tx(&bars[BAR_G], 32768);
+    tma_load_3d(sm + SM_QAKA, &p.tm_g, &bars[BAR_G], 0, h, r0);
   };
   auto load_beta = [&](int cidx) {
     const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
     const int valid = min(kChunk, w.len - cidx * kChunk);
     beta_next = (ptid < valid) ? p.beta[(row0 + ptid) * H + h] : 0.f;
   };
-  if (ptid == 0) issue_qk(p, w, sm, bars, w.c0);
-  load_g(w.c0, 0, 4);
+  if (ptid == 0) { issue_qk(p, w, sm, bars, w.c0); issue_g(w.c0); }
   if (ptid < kChunk) load_beta(w.c0);
 
   for (int n = 0; n < n_chunks; ++n) {
@@ -391,7 +404,6 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     const bool has_next = (n + 1) < n_chunks;
     if (ptid == 0 && has_next) {  // pull the next chunk's tiles toward L2
       const int rn = static_cast<int>(w.bos + static_cast<int64_t>(cidx + 1) * kChunk);
-      tma_prefetch_3d(&p.tm_g, 0, h, rn);
       tma_prefetch_3d(&p.tm_q, 0, h, rn); tma_prefetch_3d(&p.tm_q, 64, h, rn);
       tma_prefetch_3d(&p.tm_k, 0, h, rn); tma_prefetch_3d(&p.tm_k, 64, h, rn);
       tma_prefetch_3d(&p.tm_v, 0, h, rn); tma_prefetch_3d(&p.tm_v, 64, h, rn);
@@ -401,12 +413,20 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     // ---- 1. cumsum of g: thread prefix over its 4 tokens, warp scan over the block's
     //         4 quads, block sums exchanged through shared memory
     float G[4][8];
+    if (!mbar_wait(&bars[BAR_G], n & 1)) ctrl[CTRL_ABORT] = 1;
+    {
+      const int valid_g = min(kChunk, w.len - cidx * kChunk);
+      const float* gt = reinterpret_cast<const float*>(sm + SM_QAKA);  // [64][128] fp32
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      G[u][0] = gx[u][0].x; G[u][1] = gx[u][0].y; G[u][2] = gx[u][0].z; G[u][3] = gx[u][0].w;
-      G[u][4] = gx[u][1].x; G[u][5] = gx[u][1].y; G[u][6] = gx[u][1].z; G[u][7] = gx[u][1].w;
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + u;
+        const float4 a = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8);
+        const float4 b = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8 + 4);
+        const bool m = t < valid_g;
+        G[u][0] = m ? a.x : 0.f; G[u][1] = m ? a.y : 0.f; G[u][2] = m ? a.z : 0.f; G[u][3] = m ? a.w : 0.f;
+        G[u][4] = m ? b.x : 0.f; G[u][5] = m ? b.y : 0.f; G[u][6] = m ? b.z : 0.f; G[u][7] = m ? b.w : 0.f;
+      }
     }
-    if (has_next) load_g(cidx + 1, 0, 2);
     if (has_next && ptid < kChunk) load_beta(cidx + 1);
 #pragma unroll
     for (int u = 1; u < 4; ++u)
@@ -499,7 +519,6 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         }
       }
     }
-    if (has_next) load_g(cidx + 1, 2, 4);
     fence_proxy_async_smem();
     named_bar_sync(kBarP, kPThreads);
     if (ptid == 0) {
@@ -512,18 +531,23 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       mma_commit(&bars[BAR_LM]);
     }
 
-    // ---- 4. L (fp32, beta-scaled) and M_qk (fp16, staged in the QA/KA region)
+    // ---- 4. L (fp32, beta-scaled) and M_qk (fp16, straight into rows 64..127 of the
+    //         [INV Diag(beta); M_qk] operand, once the previous chunk's update is done)
     if (!mbar_wait(&bars[BAR_LM], n & 1)) ctrl[CTRL_ABORT] = 1;
     tc_fence_after();
-    if (pw < 4) {
-      const int q = pw;  // TMEM lane quarter
+    if (ptid == 0 && has_next) issue_g(cidx + 1);  // QA / KA consumed: the region takes the next g
+    if (n > 0 && !mbar_wait(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
+    {
+      const int q = pw & 3, part = pw >> 2;  // TMEM lane quarter; two warps split its columns
       const bool is_l = q >= 2;
       const int t = (q & 1) * 32 + lane;
       const int tbl = t >> 4;
-      const int g0 = (q & 1) ? 3 : 0, ng = (q & 1) ? 7 : 3;
+      const int g0 = (q & 1) ? 3 : 0, ng = (q & 1) ? 7 : 3, nh = (ng + 1) >> 1;
+      const int gb = part ? nh : 0, ge = part ? ng : nh;
       const int lo = static_cast<int>(lm_col(tbl)), hi = lo + 16 * (tbl + 1);
       const float bt = s_beta[t];
-      for (int gi = 0; gi < ng; ++gi) {
+      uint8_t* mp = sm + SM_IM + 8192;  // M_qk rows share the swizzle phase of rows 0..63
+      for (int gi = gb; gi < ge; ++gi) {
         float r[16];
         tmem_ld16(tmem + tl + kTLM + (g0 + gi) * 16, r);
         tmem_wait_ld();
@@ -541,21 +565,22 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
           float v[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = (s0 + e <= t) ? r[e] : 0.f;
-          uint8_t* mp = sm + SM_QAKA;
           st4(mp + sw128(t, 2 * s0), pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
               pack_half2(v[6], v[7]));
           st4(mp + sw128(t, 2 * s0 + 16), pack_half2(v[8], v[9]), pack_half2(v[10], v[11]), pack_half2(v[12], v[13]),
               pack_half2(v[14], v[15]));
         }
       }
-      for (int sb = tbl + 1; sb < 4; ++sb) {
-        if (is_l) {
-          float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + sb * 16;
+      if (part == 0) {
+        for (int sb = tbl + 1; sb < 4; ++sb) {
+          if (is_l) {
+            float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + sb * 16;
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(wr + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          st4(sm + SM_QAKA + sw128(t, 32 * sb), 0, 0, 0, 0);
-          st4(sm + SM_QAKA + sw128(t, 32 * sb + 16), 0, 0, 0, 0);
+            for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(wr + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            st4(mp + sw128(t, 32 * sb), 0, 0, 0, 0);
+            st4(mp + sw128(t, 32 * sb + 16), 0, 0, 0, 0);
+          }
         }
       }
     }
@@ -565,15 +590,8 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     invert_unit_lower(reinterpret_cast<const float*>(sm + SM_WL), reinterpret_cast<float*>(sm + SM_WI),
                       reinterpret_cast<float*>(sm + SM_PT), ptid);
 
-    // ---- 6. [INV Diag(beta); M_qk] and K_restore once the previous state update is done
-    if (n > 0 && !mbar_wait(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
-    put_inv_beta(reinterpret_cast<const float*>(sm + SM_WI), reinterpret_cast<const float*>(sm + SM_PT), s_beta,
-                 sm + SM_IM, ptid);
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {  // M_qk rows: 8 KiB copied to rows 64..127 (same swizzle phase)
-      const int o = (ptid * 2 + c) * 16;
-      *reinterpret_cast<uint4*>(sm + SM_IM + 8192 + o) = *reinterpret_cast<const uint4*>(sm + SM_QAKA + o);
-    }
+    // ---- 6. INV Diag(beta) and K_restore (their buffers were released before step 4)
+    put_inv_beta(reinterpret_cast<const float*>(sm + SM_WI), s_beta, sm + SM_IM, ptid);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       st4(sm + SM_KR + kpanel * 8192 + sw128(t0 + u, 16 * kchunk), krq[u][0], krq[u][1], krq[u][2], krq[u][3]);
@@ -590,7 +608,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
 // all 128 lanes.
 __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                                 uint32_t tmem, int n_chunks, bool do_o, bool v_zero, bool entry_identity, int tid) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
   const int rw = tid >> 5;
   const uint32_t tl = static_cast<uint32_t>(rw * 32) << 16;
   const uint64_t dS16 = smem_desc(smem_u32(sm + SM_S16), 16384, 1024, kSwizzle128B);
