@@ -56,6 +56,7 @@ constexpr int kRThreads = 128;  // recurrent group: warps 0-3 (TMEM lane quarter
 constexpr int kPThreads = 256;  // prep group: warps 4-11
 constexpr uint32_t kBarR = 1, kBarP = 2;  // named barrier ids
 constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM columns (all 128-lane layouts: lane = row of D).
 //   TS  [0, 128)   the state S, fp32 (lane = d_k row)
@@ -77,7 +78,7 @@ constexpr uint32_t SM_MISC = 221184;
 constexpr uint32_t SM_WL = SM_BT;              // fp32 [64][68] L        (over B_tb, once consumed)
 constexpr uint32_t SM_WI = SM_BT + 17408;      // fp32 [64][68] INV
 constexpr uint32_t SM_PT = SM_BT + 34816;      // fp32 4 x [16][20] block scratch (ends at SM_BT + 39936)
-constexpr uint32_t SM_TOT = SM_MISC;           // fp32 [4][128] per-block sums of g (prep)
+constexpr uint32_t SM_TOT = SM_MISC;           // fp32 [4][128] per-block total decay 2^(sum of G) (prep)
 constexpr uint32_t SM_AL = SM_TOT + 7168;      // fp32 [2][128] a_last by chunk parity (prep -> recurrent)
 constexpr uint32_t SM_BETA = SM_AL + 1024;     // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;     // mbarriers
@@ -176,150 +177,140 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
 
 // ------------------------------------------------------------- INV = (I + L)^-1
 // L is 64 x 64 strictly lower triangular, fp32 in shared memory with row stride kLdw.
-// Block forward substitution over 16 x 16 blocks (D_i = (I + L_ii)^-1):
-//     INV_ii = D_i,   INV_ij = -D_i (L_ij D_j + sum_{j<k<i} L_ik INV_kj)   (i > j)
-// evaluated in dependency stages, one warp per 16 x 16 block product.
-constexpr int kLdw = 68;  // padded row stride (floats): conflict-free float4 row reads
-constexpr int kLdp = 20;  // row stride of the 16 x 16 scratch blocks (conflict-free 8-row reads)
+// With D = blockdiag((I + L_ii)^-1) over 16 x 16 blocks and N = D L_off (strictly block
+// lower, so N^4 = 0):  I + L = blockdiag(I + L_ii) (I + N)  =>  INV = (I - N + N^2 - N^3) D.
+constexpr int kLdw = 68;  // padded row stride (floats) of L and INV
+constexpr int kLdp = 20;  // row stride of the 16 x 16 scratch blocks
+
+// 16 x 16 x 16 block products on the warp's tensor path (mma.sync m16n8k8, tf32) with the
+// operands split into high and low tf32 parts and the three significant cross products
+// summed (hi hi + hi lo + lo hi): fp32-level accuracy from 10-bit-mantissa operands.
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Operand A of a block product: A0 - A1 - A2 (A1, A2 optional), fp32 blocks in shared memory.
+struct BlkA {
+  const float* a0; int ld0;
+  const float* a1; int ld1;
+  const float* a2; int ld2;
+  __device__ __forceinline__ float at(int r, int c) const {
+    float v = a0[r * ld0 + c];
+    if (a1) v -= a1[r * ld1 + c];
+    if (a2) v -= a2[r * ld2 + c];
+    return v;
+  }
+};
+// acc += A B for one warp.  Fragments (PTX m16n8k8 .tf32): g = lane / 4, q = lane % 4;
+// A rows g, g + 8, columns q, q + 4 of each 8-wide k step; B rows q, q + 4, column g of
+// each 8-wide n half; acc[h] holds C rows g (0, 1) and g + 8 (2, 3), columns 8 h + 2 q (+1).
+__device__ __forceinline__ void blk_mma(const BlkA& A, const float* B, int ldb, float (&acc)[2][4], int lane) {
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int k0 = 0; k0 < 16; k0 += 8) {
+    uint32_t ah[4], al[4];
+    tf32_split(A.at(g, k0 + q), ah[0], al[0]);
+    tf32_split(A.at(g + 8, k0 + q), ah[1], al[1]);
+    tf32_split(A.at(g, k0 + q + 4), ah[2], al[2]);
+    tf32_split(A.at(g + 8, k0 + q + 4), ah[3], al[3]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t bh0, bl0, bh1, bl1;
+      tf32_split(B[(k0 + q) * ldb + 8 * h + g], bh0, bl0);
+      tf32_split(B[(k0 + q + 4) * ldb + 8 * h + g], bh1, bl1);
+      mma_tf32(acc[h], al, bh0, bh1);
+      mma_tf32(acc[h], ah, bl0, bl1);
+      mma_tf32(acc[h], ah, bh0, bh1);
+    }
+  }
+}
+__device__ __forceinline__ void blk_store(float* C, int ldc, const float (&acc)[2][4], int lane, float sign) {
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    *reinterpret_cast<float2*>(C + g * ldc + 8 * h + 2 * q) = make_float2(sign * acc[h][0], sign * acc[h][1]);
+    *reinterpret_cast<float2*>(C + (g + 8) * ldc + 8 * h + 2 * q) = make_float2(sign * acc[h][2], sign * acc[h][3]);
+  }
+}
 
 // Called by the 256 prep threads (ptid 0..255); synchronises the prep group only.
-// INV = (I + L)^-1 for L strictly lower (64 x 64, fp32, row stride kLdw in WL), by 16 x 16
-// blocks: with D = blockdiag((I + L_ii)^-1) and N = D L_off (strictly block-lower, N^4 = 0),
-//     (I + L) = blockdiag(I + L_ii) (I + N)  =>  INV = (I - N + N^2 - N^3) D.
-// On return WI holds INV (all blocks, upper blocks not written: the reader masks them).
-// `half`-warp products: a 16 x 16 x 16 product is split over two warps (8 rows each).
-__device__ __forceinline__ void blk_mac8(const float* A, int lda, const float* B, int ldb, float (&acc)[4], int lane,
-                                         int rbase) {
-  const int r = rbase + (lane >> 2), c0 = (lane & 3) * 4;
-  float a[16];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 v = *reinterpret_cast<const float4*>(A + r * lda + 4 * q);
-    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
-  }
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float4 b = *reinterpret_cast<const float4*>(B + k * ldb + c0);
-    acc[0] += a[k] * b.x; acc[1] += a[k] * b.y; acc[2] += a[k] * b.z; acc[3] += a[k] * b.w;
-  }
-}
-__device__ __forceinline__ void blk_ld8(const float* C, int ldc, float (&acc)[4], int lane, int rbase, float sign) {
-  const float4 x = *reinterpret_cast<const float4*>(C + (rbase + (lane >> 2)) * ldc + (lane & 3) * 4);
-  acc[0] = sign * x.x; acc[1] = sign * x.y; acc[2] = sign * x.z; acc[3] = sign * x.w;
-}
-__device__ __forceinline__ void blk_st8(float* C, int ldc, const float (&acc)[4], int lane, int rbase, float sign) {
-  *reinterpret_cast<float4*>(C + (rbase + (lane >> 2)) * ldc + (lane & 3) * 4) =
-      make_float4(sign * acc[0], sign * acc[1], sign * acc[2], sign * acc[3]);
-}
-
+// On return WI holds INV on and below the block diagonal (the reader masks the rest).
 __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int ptid) {
   const int warp = ptid >> 5, lane = ptid & 31;
   auto L = [&](int i, int j) { return WL + 16 * i * kLdw + 16 * j; };
   auto I = [&](int i, int j) { return WI + 16 * i * kLdw + 16 * j; };
   auto P = [&](int k) { return PT + 320 * k; };  // 16 x 16 blocks, row stride kLdp
 
-  // D_b: thread (b, c) solves column c of (I + L_bb) x = e_c  -> WI(b, b)
+  // D_b = (I + L_bb)^-1: thread (b, c) forms column c by forward substitution, pushing
+  // each finished x[m] into the rows below it (a 15-step dependency chain).
   if (ptid < 64) {
     const int b = ptid >> 4, c = ptid & 15;
     const float* Lb = L(b, b);
     float x[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float s = 0.f;
+    for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < r; ++m) s += Lb[r * kLdw + m] * x[m];
-      x[r] = (r == c) ? 1.f : (r < c ? 0.f : -s);
-    }
+    for (int m = 0; m < 15; ++m)
+#pragma unroll
+      for (int r = m + 1; r < 16; ++r) x[r] -= Lb[r * kLdw + m] * x[m];
     float* Db = I(b, b);
 #pragma unroll
     for (int r = 0; r < 16; ++r) Db[r * kLdw + c] = x[r];
   }
   named_bar_sync(kBarP, kPThreads);
-  // N_ij = D_i L_ij for (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) -> WI(i, j); 6 products, 8 warps
-  // (warps 0-5 one product each; warps 6, 7 split (3,0) with... kept simple: one warp per product)
+  // N_ij = D_i L_ij for (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) -> WI(i, j): warps 0-5
   if (warp < 6) {
     const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
     const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
-    float a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
-    blk_mac8(I(i, i), kLdw, L(i, j), kLdw, a0, lane, 0);
-    blk_mac8(I(i, i), kLdw, L(i, j), kLdw, a1, lane, 8);
-    blk_st8(I(i, j), kLdw, a0, lane, 0, 1.f);
-    blk_st8(I(i, j), kLdw, a1, lane, 8, 1.f);
+    float acc[2][4] = {};
+    blk_mma(BlkA{I(i, i), kLdw, nullptr, 0, nullptr, 0}, L(i, j), kLdw, acc, lane);
+    blk_store(I(i, j), kLdw, acc, lane, 1.f);
   }
   named_bar_sync(kBarP, kPThreads);
-  // second-order terms (two warps per product, 8 rows each):
-  //   P0 = N_21 N_10, P1 = N_32 N_21, P2 = N_31 N_10 + N_32 N_20
-  {
-    const int prod = warp >> 1, rb = (warp & 1) * 8;
-    if (prod == 0) {
-      float a[4] = {0, 0, 0, 0};
-      blk_mac8(I(2, 1), kLdw, I(1, 0), kLdw, a, lane, rb);
-      blk_st8(P(0), kLdp, a, lane, rb, 1.f);
-    } else if (prod == 1) {
-      float a[4] = {0, 0, 0, 0};
-      blk_mac8(I(3, 2), kLdw, I(2, 1), kLdw, a, lane, rb);
-      blk_st8(P(1), kLdp, a, lane, rb, 1.f);
-    } else if (prod == 2) {
-      float a[4] = {0, 0, 0, 0};
-      blk_mac8(I(3, 1), kLdw, I(1, 0), kLdw, a, lane, rb);
-      blk_mac8(I(3, 2), kLdw, I(2, 0), kLdw, a, lane, rb);
-      blk_st8(P(2), kLdp, a, lane, rb, 1.f);
-    }
+  // second and third order: P0 = N_21 N_10, P1 = N_32 N_21, P2 = N_31 N_10 + N_32 N_20,
+  // P3 = P1 N_10 (= N_32 N_21 N_10)
+  if (warp == 0) {
+    float acc[2][4] = {};
+    blk_mma(BlkA{I(2, 1), kLdw, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc, lane);
+    blk_store(P(0), kLdp, acc, lane, 1.f);
+  } else if (warp == 1) {
+    float acc[2][4] = {};
+    blk_mma(BlkA{I(3, 2), kLdw, nullptr, 0, nullptr, 0}, I(2, 1), kLdw, acc, lane);
+    blk_store(P(1), kLdp, acc, lane, 1.f);
+    __syncwarp();
+    float acc3[2][4] = {};
+    blk_mma(BlkA{P(1), kLdp, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc3, lane);
+    blk_store(P(3), kLdp, acc3, lane, 1.f);
+  } else if (warp == 2) {
+    float acc[2][4] = {};
+    blk_mma(BlkA{I(3, 1), kLdw, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc, lane);
+    blk_mma(BlkA{I(3, 2), kLdw, nullptr, 0, nullptr, 0}, I(2, 0), kLdw, acc, lane);
+    blk_store(P(2), kLdp, acc, lane, 1.f);
   }
   named_bar_sync(kBarP, kPThreads);
-  // M = -N + N^2 - N^3 (strictly block lower) into P(.) / WI:
-  //   M_10 = -N_10, M_21 = -N_21, M_32 = -N_32 (negated in the last stage)
-  //   M_20 = -N_20 + P0 -> P(0) ; M_31 = -N_31 + P1 -> P(1) ; M_30 = -N_30 + P2 - N_32 P0 -> P(2)
-  {
-    const int task = warp >> 1, rb = (warp & 1) * 8;
-    if (task == 0) {
-      float a[4];
-      blk_ld8(P(0), kLdp, a, lane, rb, 1.f);
-      float n[4];
-      blk_ld8(I(2, 0), kLdw, n, lane, rb, 1.f);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) a[e] -= n[e];
-      blk_st8(P(3), kLdp, a, lane, rb, 1.f);  // M_20 (P(0) is still read by task 2)
-    } else if (task == 1) {
-      float a[4];
-      blk_ld8(P(1), kLdp, a, lane, rb, 1.f);
-      float n[4];
-      blk_ld8(I(3, 1), kLdw, n, lane, rb, 1.f);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) a[e] -= n[e];
-      blk_st8(P(1), kLdp, a, lane, rb, 1.f);  // M_31 in place (own elements only)
-    } else if (task == 2) {
-      float a[4];
-      blk_ld8(P(2), kLdp, a, lane, rb, 1.f);
-      float n[4];
-      blk_ld8(I(3, 0), kLdw, n, lane, rb, 1.f);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) a[e] -= n[e];
-      float c[4] = {0, 0, 0, 0};
-      blk_mac8(I(3, 2), kLdw, P(0), kLdp, c, lane, rb);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) a[e] -= c[e];
-      blk_st8(P(2), kLdp, a, lane, rb, 1.f);  // M_30 in place (own elements only)
-    }
-  }
-  named_bar_sync(kBarP, kPThreads);
-  // INV_ij = M_ij D_j: six products, warps 0-5 (16 rows each as two 8-row halves)
+  // INV_ij = M_ij D_j with M = -N + N^2 - N^3 (strictly block lower):
+  //   M_10 = -N_10, M_21 = -N_21, M_32 = -N_32, M_20 = P0 - N_20, M_31 = P1 - N_31,
+  //   M_30 = P2 - N_30 - P3.   Each warp overwrites only the N block it reads.
   if (warp < 6) {
     const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
     const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
-    const float* M;
-    int ldm;
-    float sgn = 1.f;
-    if (i == j + 1) { M = I(i, j); ldm = kLdw; sgn = -1.f; }  // M = -N on the first sub-diagonal
-    else if (i == 2) { M = P(3); ldm = kLdp; }                   // (2,0)
-    else if (j == 1) { M = P(1); ldm = kLdp; }                   // (3,1)
-    else { M = P(2); ldm = kLdp; }                               // (3,0)
-    float a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
-    blk_mac8(M, ldm, I(j, j), kLdw, a0, lane, 0);
-    blk_mac8(M, ldm, I(j, j), kLdw, a1, lane, 8);
-    __syncwarp();  // every lane has read its rows of M (this warp's block only) before the store
-    blk_st8(I(i, j), kLdw, a0, lane, 0, sgn);
-    blk_st8(I(i, j), kLdw, a1, lane, 8, sgn);
+    BlkA m{I(i, j), kLdw, nullptr, 0, nullptr, 0};
+    float sgn = -1.f;
+    if (i == 2 && j == 0) { m = BlkA{P(0), kLdp, I(2, 0), kLdw, nullptr, 0}; sgn = 1.f; }
+    if (i == 3 && j == 1) { m = BlkA{P(1), kLdp, I(3, 1), kLdw, nullptr, 0}; sgn = 1.f; }
+    if (i == 3 && j == 0) { m = BlkA{P(2), kLdp, I(3, 0), kLdw, P(3), kLdp}; sgn = 1.f; }
+    float acc[2][4] = {};
+    blk_mma(m, I(j, j), kLdw, acc, lane);
+    __syncwarp();  // every lane has read its operands before the block is overwritten
+    blk_store(I(i, j), kLdw, acc, lane, sgn);
   }
   named_bar_sync(kBarP, kPThreads);
 }
@@ -379,7 +370,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
   const int H = p.H, h = w.h;
   const uint32_t tl = static_cast<uint32_t>((pw & 3) * 32) << 16;
   float* s_beta = reinterpret_cast<float*>(sm + SM_BETA);
-  float* tot = reinterpret_cast<float*>(sm + SM_TOT);  // [4][128] per-block sums of g
+  float* tot = reinterpret_cast<float*>(sm + SM_TOT);  // [4][128] per-block total decay 2^(sum of G)
   const uint64_t dQAKA = smem_desc(smem_u32(sm + SM_QAKA), 16, 1024, kSwizzle128B);
   const uint64_t dBT = smem_desc(smem_u32(sm + SM_BT), 16, 1024, kSwizzle128B);
   const uint32_t id_lm = idesc_f16(128, 160, true, false, false);
@@ -391,10 +382,10 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     mbar_arrive_expect_tx(&bars[BAR_G], 32768);
     tma_load_3d(sm + SM_QAKA, &p.tm_g, &bars[BAR_G], 0, h, r0);
   };
-  auto load_beta = [&](int cidx) {
+  auto load_beta = [&](int cidx) {  // in-bounds row, masked when stored: the load never blocks
     const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
     const int valid = min(kChunk, w.len - cidx * kChunk);
-    beta_next = (ptid < valid) ? p.beta[(row0 + ptid) * H + h] : 0.f;
+    beta_next = p.beta[(row0 + min(ptid, valid - 1)) * H + h];
   };
   if (ptid == 0) { issue_qk(p, w, sm, bars, w.c0); issue_g(w.c0); }
   if (ptid < kChunk) load_beta(w.c0);
@@ -408,10 +399,11 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       tma_prefetch_3d(&p.tm_k, 0, h, rn); tma_prefetch_3d(&p.tm_k, 64, h, rn);
       tma_prefetch_3d(&p.tm_v, 0, h, rn); tma_prefetch_3d(&p.tm_v, 64, h, rn);
     }
-    if (ptid < kChunk) s_beta[ptid] = beta_next;
+    if (ptid < kChunk) s_beta[ptid] = ptid < min(kChunk, w.len - cidx * kChunk) ? beta_next : 0.f;
 
-    // ---- 1. cumsum of g: thread prefix over its 4 tokens, warp scan over the block's
-    //         4 quads, block sums exchanged through shared memory
+    // ---- 1. cumsum of g in log2 units (G = log2(e) x sum g): thread prefix over its 4
+    //         tokens, warp scan over the block's 4 quads.  The block's total decay
+    //         A[tb] = 2^(block sum) goes to shared memory for the other blocks' factors.
     float G[4][8];
     if (!mbar_wait(&bars[BAR_G], n & 1)) ctrl[CTRL_ABORT] = 1;
     {
@@ -422,9 +414,9 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         const int t = t0 + u;
         const float4 a = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8);
         const float4 b = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8 + 4);
-        const bool m = t < valid_g;
-        G[u][0] = m ? a.x : 0.f; G[u][1] = m ? a.y : 0.f; G[u][2] = m ? a.z : 0.f; G[u][3] = m ? a.w : 0.f;
-        G[u][4] = m ? b.x : 0.f; G[u][5] = m ? b.y : 0.f; G[u][6] = m ? b.z : 0.f; G[u][7] = m ? b.w : 0.f;
+        const float m = t < valid_g ? kLog2e : 0.f;
+        G[u][0] = m * a.x; G[u][1] = m * a.y; G[u][2] = m * a.z; G[u][3] = m * a.w;
+        G[u][4] = m * b.x; G[u][5] = m * b.y; G[u][6] = m * b.z; G[u][7] = m * b.w;
       }
     }
     if (has_next && ptid < kChunk) load_beta(cidx + 1);
@@ -432,6 +424,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     for (int u = 1; u < 4; ++u)
 #pragma unroll
       for (int e = 0; e < 8; ++e) G[u][e] += G[u - 1][e];
+    float A[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       float run = G[3][e];
@@ -442,28 +435,45 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       const float excl = run - G[3][e];
 #pragma unroll
       for (int u = 0; u < 4; ++u) G[u][e] += excl;  // block-local inclusive cumsum
-      if (tql == 3) tot[tb * 128 + cg * 8 + e] = G[3][e];
+      A[e] = exp2_fast(G[3][e]);
+    }
+    if (tql == 3) {
+      float4* dst = reinterpret_cast<float4*>(tot + tb * 128 + cg * 8);
+      dst[0] = make_float4(A[0], A[1], A[2], A[3]);
+      dst[1] = make_float4(A[4], A[5], A[6], A[7]);
     }
     named_bar_sync(kBarP, kPThreads);
 
-    // ---- 2. block references Gx[b] (sum of earlier blocks), G_last, decay factors.
-    //         G stays block-local: E = exp(G) = a / a(Gx[tb]) <= 1.
+    // ---- 2. decay factors as products of the block totals A[0..3]:
+    //         atr = 2^Gx[tb] (chunk start -> block reference), rtr = 2^(G_last - Gx[tb]),
+    //         fr[j] = 2^(Gx[tb + 1 + j] - Gx[tb]) (<= 1) for the later row blocks.
     float atr[8], rtr[8], fr[3][8];
     {
-      const int c = cg * 8;
+      float a[4][8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float4 x = *reinterpret_cast<const float4*>(tot + b * 128 + cg * 8);
+        const float4 y = *reinterpret_cast<const float4*>(tot + b * 128 + cg * 8 + 4);
+        a[b][0] = x.x; a[b][1] = x.y; a[b][2] = x.z; a[b][3] = x.w;
+        a[b][4] = y.x; a[b][5] = y.y; a[b][6] = y.z; a[b][7] = y.w;
+      }
+      float al[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float s0 = tot[0 * 128 + c + e], s1 = tot[1 * 128 + c + e], s2 = tot[2 * 128 + c + e],
-                    s3 = tot[3 * 128 + c + e];
-        const float gx1 = s0, gx2 = s0 + s1, gx3 = s0 + s1 + s2, gl = gx3 + s3;
-        const float own = tb == 0 ? 0.f : tb == 1 ? gx1 : tb == 2 ? gx2 : gx3;
-        atr[e] = __expf(own);       // decay from the chunk start to the block reference
-        rtr[e] = __expf(gl - own);  // decay from the block reference to the chunk end
-        // F for the later row blocks b2 = tb + 1 .. 3: exp(Gx[b2] - Gx[tb]) <= 1
-        fr[0][e] = tb < 3 ? __expf((tb == 0 ? gx1 : tb == 1 ? gx2 : gx3) - own) : 0.f;
-        fr[1][e] = tb < 2 ? __expf((tb == 0 ? gx2 : gx3) - own) : 0.f;
-        fr[2][e] = tb < 1 ? __expf(gx3 - own) : 0.f;
-        if (tb == 0 && tql == 0) reinterpret_cast<float*>(sm + SM_AL)[(n & 1) * 128 + c + e] = __expf(gl);
+        const float a0 = a[0][e], a1 = a[1][e], a2 = a[2][e], a3 = a[3][e];
+        const float p01 = a0 * a1, p12 = a1 * a2, p23 = a2 * a3;
+        const float p012 = p01 * a2, p123 = p12 * a3;
+        al[e] = p012 * a3;
+        atr[e] = tb == 0 ? 1.f : tb == 1 ? a0 : tb == 2 ? p01 : p012;
+        rtr[e] = tb == 0 ? al[e] : tb == 1 ? p123 : tb == 2 ? p23 : a3;
+        fr[0][e] = tb == 0 ? a0 : tb == 1 ? a1 : tb == 2 ? a2 : 0.f;
+        fr[1][e] = tb == 0 ? p01 : tb == 1 ? p12 : 0.f;
+        fr[2][e] = tb == 0 ? p012 : 0.f;
+      }
+      if (tb == 0 && tql == 0) {
+        float4* dst = reinterpret_cast<float4*>(sm + SM_AL) + ((n & 1) * 128 + cg * 8) / 4;
+        dst[0] = make_float4(al[0], al[1], al[2], al[3]);
+        dst[1] = make_float4(al[4], al[5], al[6], al[7]);
       }
     }
 
@@ -489,8 +499,8 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float kk = m ? kf[e] : 0.f;
-          const float E = __expf(G[u][e]);    // in [e^-80, 1]
-          const float Ei = __expf(-G[u][e]);  // in [1, e^80]
+          const float E = exp2_fast(G[u][e]);    // in [e^-80, 1]
+          const float Ei = exp2_fast(-G[u][e]);  // in [1, e^80]
           qa[e] = qf[e] * E;
           ka[e] = kk * E;
           kb[e] = kk * Ei;

@@ -233,6 +233,15 @@ __host__ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t b) {
   return r * 128u + ((((b >> 4) ^ (r & 7u)) << 4) | (b & 15u));
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative error about
+// 2^-22; results below 2^-126 flush to zero).  Callers carry exponents in log2 units, so
+// e^y is exp2_fast(y * log2(e)).
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
