@@ -57,6 +57,9 @@ constexpr int kPThreads = 256;  // prep group: warps 4-11
 constexpr uint32_t kBarR = 1, kBarP = 2;  // named barrier ids
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+// Block totals table: [4 blocks][16 channel groups], 12 floats per group (8 used), so the
+// eight 32-byte groups an 8-lane phase reads fall on distinct banks.
+constexpr int kTotCg = 12, kTotPitch = 16 * kTotCg;
 
 // TMEM columns (all 128-lane layouts: lane = row of D).
 //   TS  [0, 128)   the state S, fp32 (lane = d_k row)
@@ -78,7 +81,7 @@ constexpr uint32_t SM_MISC = 221184;
 constexpr uint32_t SM_WL = SM_BT;              // fp32 [64][68] L        (over B_tb, once consumed)
 constexpr uint32_t SM_WI = SM_BT + 17408;      // fp32 [64][68] INV
 constexpr uint32_t SM_PT = SM_BT + 34816;      // fp32 4 x [16][20] block scratch (ends at SM_BT + 39936)
-constexpr uint32_t SM_TOT = SM_MISC;           // fp32 [4][128] per-block total decay 2^(sum of G) (prep)
+constexpr uint32_t SM_TOT = SM_MISC;           // fp32 [4][16][12] per-block total decay 2^(sum of G) (prep)
 constexpr uint32_t SM_AL = SM_TOT + 7168;      // fp32 [2][128] a_last by chunk parity (prep -> recurrent)
 constexpr uint32_t SM_BETA = SM_AL + 1024;     // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;     // mbarriers
@@ -182,13 +185,13 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
 constexpr int kLdw = 68;  // padded row stride (floats) of L and INV
 constexpr int kLdp = 20;  // row stride of the 16 x 16 scratch blocks
 
-// 16 x 16 x 16 block products on the warp's tensor path (mma.sync m16n8k8, tf32) with the
-// operands split into high and low tf32 parts and the three significant cross products
-// summed (hi hi + hi lo + lo hi): fp32-level accuracy from 10-bit-mantissa operands.
-__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-  const float r = x - __uint_as_float(hi);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+// 16 x 16 x 16 block products on the warp's tensor path (mma.sync m16n8k8, tf32 operands
+// rounded to nearest, fp32 accumulation).  The operands carry 11 significant bits, the
+// precision INV keeps anyway once it is rounded to the fp16 operand of U = INV Diag(beta) X.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
 }
 __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -197,39 +200,33 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// Operand A of a block product: A0 - A1 - A2 (A1, A2 optional), fp32 blocks in shared memory.
+// Operand A of a block product: A0 - A1 - A2 with the first NT terms present (NT fixed at
+// compile time, so the element loads carry no branches), fp32 blocks in shared memory.
+template <int NT>
 struct BlkA {
   const float* a0; int ld0;
   const float* a1; int ld1;
   const float* a2; int ld2;
   __device__ __forceinline__ float at(int r, int c) const {
     float v = a0[r * ld0 + c];
-    if (a1) v -= a1[r * ld1 + c];
-    if (a2) v -= a2[r * ld2 + c];
+    if (NT > 1) v -= a1[r * ld1 + c];
+    if (NT > 2) v -= a2[r * ld2 + c];
     return v;
   }
 };
 // acc += A B for one warp.  Fragments (PTX m16n8k8 .tf32): g = lane / 4, q = lane % 4;
 // A rows g, g + 8, columns q, q + 4 of each 8-wide k step; B rows q, q + 4, column g of
 // each 8-wide n half; acc[h] holds C rows g (0, 1) and g + 8 (2, 3), columns 8 h + 2 q (+1).
-__device__ __forceinline__ void blk_mma(const BlkA& A, const float* B, int ldb, float (&acc)[2][4], int lane) {
+template <int NT>
+__device__ __forceinline__ void blk_mma(const BlkA<NT>& A, const float* B, int ldb, float (&acc)[2][4], int lane) {
   const int g = lane >> 2, q = lane & 3;
 #pragma unroll
   for (int k0 = 0; k0 < 16; k0 += 8) {
-    uint32_t ah[4], al[4];
-    tf32_split(A.at(g, k0 + q), ah[0], al[0]);
-    tf32_split(A.at(g + 8, k0 + q), ah[1], al[1]);
-    tf32_split(A.at(g, k0 + q + 4), ah[2], al[2]);
-    tf32_split(A.at(g + 8, k0 + q + 4), ah[3], al[3]);
+    const uint32_t a[4] = {to_tf32(A.at(g, k0 + q)), to_tf32(A.at(g + 8, k0 + q)), to_tf32(A.at(g, k0 + q + 4)),
+                           to_tf32(A.at(g + 8, k0 + q + 4))};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t bh0, bl0, bh1, bl1;
-      tf32_split(B[(k0 + q) * ldb + 8 * h + g], bh0, bl0);
-      tf32_split(B[(k0 + q + 4) * ldb + 8 * h + g], bh1, bl1);
-      mma_tf32(acc[h], al, bh0, bh1);
-      mma_tf32(acc[h], ah, bl0, bl1);
-      mma_tf32(acc[h], ah, bh0, bh1);
-    }
+    for (int h = 0; h < 2; ++h)
+      mma_tf32(acc[h], a, to_tf32(B[(k0 + q) * ldb + 8 * h + g]), to_tf32(B[(k0 + q + 4) * ldb + 8 * h + g]));
   }
 }
 __device__ __forceinline__ void blk_store(float* C, int ldc, const float (&acc)[2][4], int lane, float sign) {
@@ -271,7 +268,7 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int pti
     const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
     const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
     float acc[2][4] = {};
-    blk_mma(BlkA{I(i, i), kLdw, nullptr, 0, nullptr, 0}, L(i, j), kLdw, acc, lane);
+    blk_mma(BlkA<1>{I(i, i), kLdw, nullptr, 0, nullptr, 0}, L(i, j), kLdw, acc, lane);
     blk_store(I(i, j), kLdw, acc, lane, 1.f);
   }
   named_bar_sync(kBarP, kPThreads);
@@ -279,20 +276,20 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int pti
   // P3 = P1 N_10 (= N_32 N_21 N_10)
   if (warp == 0) {
     float acc[2][4] = {};
-    blk_mma(BlkA{I(2, 1), kLdw, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc, lane);
+    blk_mma(BlkA<1>{I(2, 1), kLdw, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc, lane);
     blk_store(P(0), kLdp, acc, lane, 1.f);
   } else if (warp == 1) {
     float acc[2][4] = {};
-    blk_mma(BlkA{I(3, 2), kLdw, nullptr, 0, nullptr, 0}, I(2, 1), kLdw, acc, lane);
+    blk_mma(BlkA<1>{I(3, 2), kLdw, nullptr, 0, nullptr, 0}, I(2, 1), kLdw, acc, lane);
     blk_store(P(1), kLdp, acc, lane, 1.f);
     __syncwarp();
     float acc3[2][4] = {};
-    blk_mma(BlkA{P(1), kLdp, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc3, lane);
+    blk_mma(BlkA<1>{P(1), kLdp, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc3, lane);
     blk_store(P(3), kLdp, acc3, lane, 1.f);
   } else if (warp == 2) {
     float acc[2][4] = {};
-    blk_mma(BlkA{I(3, 1), kLdw, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc, lane);
-    blk_mma(BlkA{I(3, 2), kLdw, nullptr, 0, nullptr, 0}, I(2, 0), kLdw, acc, lane);
+    blk_mma(BlkA<1>{I(3, 1), kLdw, nullptr, 0, nullptr, 0}, I(1, 0), kLdw, acc, lane);
+    blk_mma(BlkA<1>{I(3, 2), kLdw, nullptr, 0, nullptr, 0}, I(2, 0), kLdw, acc, lane);
     blk_store(P(2), kLdp, acc, lane, 1.f);
   }
   named_bar_sync(kBarP, kPThreads);
@@ -302,13 +299,12 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int pti
   if (warp < 6) {
     const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3;
     const int j = warp < 1 ? 0 : warp < 3 ? warp - 1 : warp - 3;
-    BlkA m{I(i, j), kLdw, nullptr, 0, nullptr, 0};
-    float sgn = -1.f;
-    if (i == 2 && j == 0) { m = BlkA{P(0), kLdp, I(2, 0), kLdw, nullptr, 0}; sgn = 1.f; }
-    if (i == 3 && j == 1) { m = BlkA{P(1), kLdp, I(3, 1), kLdw, nullptr, 0}; sgn = 1.f; }
-    if (i == 3 && j == 0) { m = BlkA{P(2), kLdp, I(3, 0), kLdw, P(3), kLdp}; sgn = 1.f; }
     float acc[2][4] = {};
-    blk_mma(m, I(j, j), kLdw, acc, lane);
+    float sgn = 1.f;
+    if (i == 2 && j == 0) blk_mma(BlkA<2>{P(0), kLdp, I(2, 0), kLdw, nullptr, 0}, I(j, j), kLdw, acc, lane);
+    else if (i == 3 && j == 1) blk_mma(BlkA<2>{P(1), kLdp, I(3, 1), kLdw, nullptr, 0}, I(j, j), kLdw, acc, lane);
+    else if (i == 3 && j == 0) blk_mma(BlkA<3>{P(2), kLdp, I(3, 0), kLdw, P(3), kLdp}, I(j, j), kLdw, acc, lane);
+    else { blk_mma(BlkA<1>{I(i, j), kLdw, nullptr, 0, nullptr, 0}, I(j, j), kLdw, acc, lane); sgn = -1.f; }
     __syncwarp();  // every lane has read its operands before the block is overwritten
     blk_store(I(i, j), kLdw, acc, lane, sgn);
   }
@@ -317,8 +313,8 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int pti
 
 // INV Diag(beta) -> fp16 K-major rows 0..63 of the [INV Diag(beta); M_qk] operand.
 __device__ void put_inv_beta(const float* WI, const float* beta, uint8_t* dst, int ptid) {
-  for (int task = ptid; task < 512; task += kPThreads) {
-    const int t = task >> 3, g = task & 7, s0 = 8 * g;
+  for (int task = ptid; task < 512; task += kPThreads) {  // consecutive lanes: consecutive rows
+    const int t = task & 63, g = task >> 6, s0 = 8 * g;
     float v[8];
     if ((g >> 1) > (t >> 4)) {
 #pragma unroll
@@ -370,7 +366,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
   const int H = p.H, h = w.h;
   const uint32_t tl = static_cast<uint32_t>((pw & 3) * 32) << 16;
   float* s_beta = reinterpret_cast<float*>(sm + SM_BETA);
-  float* tot = reinterpret_cast<float*>(sm + SM_TOT);  // [4][128] per-block total decay 2^(sum of G)
+  float* tot = reinterpret_cast<float*>(sm + SM_TOT);  // per-block total decay 2^(sum of G), padded
   const uint64_t dQAKA = smem_desc(smem_u32(sm + SM_QAKA), 16, 1024, kSwizzle128B);
   const uint64_t dBT = smem_desc(smem_u32(sm + SM_BT), 16, 1024, kSwizzle128B);
   const uint32_t id_lm = idesc_f16(128, 160, true, false, false);
@@ -409,11 +405,15 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     {
       const int valid_g = min(kChunk, w.len - cidx * kChunk);
       const float* gt = reinterpret_cast<const float*>(sm + SM_QAKA);  // [64][128] fp32
+      // Lanes 4-7 of each 8-lane phase read their second 16 bytes first, so every 128-bit
+      // load touches 32 distinct banks (the 32-byte lane stride alone would pair them up).
+      const int sw = (lane >> 2) & 1;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = t0 + u;
-        const float4 a = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8);
-        const float4 b = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8 + 4);
+        const float4 x = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8 + 4 * sw);
+        const float4 y = *reinterpret_cast<const float4*>(gt + t * 128 + cg * 8 + 4 * (sw ^ 1));
+        const float4 a = sw ? y : x, b = sw ? x : y;
         const float m = t < valid_g ? kLog2e : 0.f;
         G[u][0] = m * a.x; G[u][1] = m * a.y; G[u][2] = m * a.z; G[u][3] = m * a.w;
         G[u][4] = m * b.x; G[u][5] = m * b.y; G[u][6] = m * b.z; G[u][7] = m * b.w;
@@ -438,7 +438,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       A[e] = exp2_fast(G[3][e]);
     }
     if (tql == 3) {
-      float4* dst = reinterpret_cast<float4*>(tot + tb * 128 + cg * 8);
+      float4* dst = reinterpret_cast<float4*>(tot + tb * kTotPitch + cg * kTotCg);
       dst[0] = make_float4(A[0], A[1], A[2], A[3]);
       dst[1] = make_float4(A[4], A[5], A[6], A[7]);
     }
@@ -452,23 +452,55 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       float a[4][8];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const float4 x = *reinterpret_cast<const float4*>(tot + b * 128 + cg * 8);
-        const float4 y = *reinterpret_cast<const float4*>(tot + b * 128 + cg * 8 + 4);
+        const float4 x = *reinterpret_cast<const float4*>(tot + b * kTotPitch + cg * kTotCg);
+        const float4 y = *reinterpret_cast<const float4*>(tot + b * kTotPitch + cg * kTotCg + 4);
         a[b][0] = x.x; a[b][1] = x.y; a[b][2] = x.z; a[b][3] = x.w;
         a[b][4] = y.x; a[b][5] = y.y; a[b][6] = y.z; a[b][7] = y.w;
       }
       float al[8];
+      // tb is uniform across the warp: one branch, then straight-line products
+      switch (tb) {
+        case 0:
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float a0 = a[0][e], a1 = a[1][e], a2 = a[2][e], a3 = a[3][e];
-        const float p01 = a0 * a1, p12 = a1 * a2, p23 = a2 * a3;
-        const float p012 = p01 * a2, p123 = p12 * a3;
-        al[e] = p012 * a3;
-        atr[e] = tb == 0 ? 1.f : tb == 1 ? a0 : tb == 2 ? p01 : p012;
-        rtr[e] = tb == 0 ? al[e] : tb == 1 ? p123 : tb == 2 ? p23 : a3;
-        fr[0][e] = tb == 0 ? a0 : tb == 1 ? a1 : tb == 2 ? a2 : 0.f;
-        fr[1][e] = tb == 0 ? p01 : tb == 1 ? p12 : 0.f;
-        fr[2][e] = tb == 0 ? p012 : 0.f;
+          for (int e = 0; e < 8; ++e) {
+            fr[0][e] = a[0][e];
+            fr[1][e] = fr[0][e] * a[1][e];
+            fr[2][e] = fr[1][e] * a[2][e];
+            al[e] = fr[2][e] * a[3][e];
+            atr[e] = 1.f;
+            rtr[e] = al[e];
+          }
+          break;
+        case 1:
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            atr[e] = a[0][e];
+            fr[0][e] = a[1][e];
+            fr[1][e] = a[1][e] * a[2][e];
+            rtr[e] = fr[1][e] * a[3][e];
+            fr[2][e] = 0.f;
+          }
+          break;
+        case 2:
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            atr[e] = a[0][e] * a[1][e];
+            fr[0][e] = a[2][e];
+            rtr[e] = a[2][e] * a[3][e];
+            fr[1][e] = 0.f;
+            fr[2][e] = 0.f;
+          }
+          break;
+        default:
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            atr[e] = a[0][e] * a[1][e] * a[2][e];
+            rtr[e] = a[3][e];
+            fr[0][e] = 0.f;
+            fr[1][e] = 0.f;
+            fr[2][e] = 0.f;
+          }
+          break;
       }
       if (tb == 0 && tql == 0) {
         float4* dst = reinterpret_cast<float4*>(sm + SM_AL) + ((n & 1) * 128 + cg * 8) / 4;
