@@ -448,6 +448,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     //         atr = 2^Gx[tb] (chunk start -> block reference), rtr = 2^(G_last - Gx[tb]),
     //         fr[j] = 2^(Gx[tb + 1 + j] - Gx[tb]) (<= 1) for the later row blocks.
     float atr[8], rtr[8], fr[3][8];
+    uint4 rq[4], rk[4];
     {
       float a[4][8];
 #pragma unroll
@@ -458,6 +459,15 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         a[b][4] = y.x; a[b][5] = y.y; a[b][6] = y.z; a[b][7] = y.w;
       }
       float al[8];
+      // raw q, k of this thread's tokens (TMA, in the [K_decay; Q_decay] buffer): issued
+      // now so their latency overlaps the factor products
+      if (!mbar_wait(&bars[BAR_QK], n & 1)) ctrl[CTRL_ABORT] = 1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint8_t* kqp = sm + SM_KQ + kpanel * 16384;
+        rq[u] = *reinterpret_cast<const uint4*>(kqp + sw128(64 + t0 + u, 16 * kchunk));
+        rk[u] = *reinterpret_cast<const uint4*>(kqp + sw128(t0 + u, 16 * kchunk));
+      }
       // tb is uniform across the warp: one branch, then straight-line products
       switch (tb) {
         case 0:
@@ -509,9 +519,8 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       }
     }
 
-    // ---- 3. scaled operands.  Raw q, k sit in the [K_decay; Q_decay] buffer (TMA) and are
-    //         replaced in place (the recurrence released that buffer before the copy).
-    if (!mbar_wait(&bars[BAR_QK], n & 1)) ctrl[CTRL_ABORT] = 1;
+    // ---- 3. scaled operands.  Raw q, k (loaded above) are replaced in place in the
+    //         [K_decay; Q_decay] buffer (the recurrence released it before the copy).
     const int valid = min(kChunk, w.len - cidx * kChunk);
     uint32_t krq[4][4];
     {
@@ -523,8 +532,8 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         const int t = t0 + u;
         const uint32_t sk = sw128(t, 16 * kchunk), sq = sw128(64 + t, 16 * kchunk);
         float qf[8], kf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(kqp + sq), qf);
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(kqp + sk), kf);
+        bf16x8_to_f32(rq[u], qf);
+        bf16x8_to_f32(rk[u], kf);
         const bool m = t < valid;
         float qa[8], ka[8], kb[8];
         uint32_t qd2[4], kd2[4], qa2[4], ka2[4];
