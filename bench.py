@@ -39,7 +39,14 @@ STATE_BYTES = D * D * 4
 DECODE_STATE_BYTES = 8 * D * D
 DECODE_IO_BYTES = 3 * 2 * D + 4 * D + 4 + 4 * D
 DECODE_FLOP = 7 * D * D
-CPU_SAMPLE_TOKENS = 2048
+CPU_SAMPLE_TOKENS = 8192  # the whole workload: about 1.5 s on 16 host cores (about 20 s of CPU work)
+# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
+# of the kernels timed here, taken on a 16-head case and scaled by the units processed
+# (both kernels' traffic grows in proportion to the heads); the capture and the command
+# that made it are summarised in profiles/.  Set to None when the kernel changes until it is
+# captured again.
+PREFILL_TRAFFIC_PER_HEAD = 190_091_776 // 16  # bytes per head of the 8192-token launch
+DECODE_TRAFFIC_PER_HEAD = 488_329_216 // 16  # bytes per head of the 256-sequence launch
 
 
 def load_peaks():
@@ -176,10 +183,10 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: B=1, H=96, T=8192, d=128 (oracle sample: first {n} tokens of every head)",
+        "config": {"workload": f"{WORKLOAD}: B=1, H=96, T=8192, d=128 (oracle: {n} tokens of every head)",
                    "global_batch": 1, "seq_len": 8192},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"first {n} of 8192 tokens, all 96 heads, fp64 per-token recurrence"},
+                         "sample": f"{n} of 8192 tokens, all 96 heads, fp64 per-token recurrence"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -291,7 +298,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, threads, th = oracle_sample(x, CPU_SAMPLE_TOKENS)
         cpu = {"value": CPU_SAMPLE_TOKENS / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {CPU_SAMPLE_TOKENS} of 8192 tokens, all 96 heads ({th} token-heads), "
+               "sample": f"the whole workload ({CPU_SAMPLE_TOKENS} tokens x 96 heads = {th} token-heads), "
                          f"fp64 per-token recurrence, {dt:.2f} s wall"}
 
     if rank == 0:
@@ -305,7 +312,8 @@ def run_ours(args, world, rank, local):
                        "l2": "inputs (1.2 GB) larger than L2 (129 MB); no flush",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": None if PREFILL_TRAFFIC_PER_HEAD is None else PREFILL_TRAFFIC_PER_HEAD * H,
                          "kernel": "prefill_kernel", "bytes_per_launch": alg_bytes,
                          "peak_source": peaks["source"],
                          "tensor": {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -314,7 +322,8 @@ def run_ours(args, world, rank, local):
             "decode": {"metric": "KDA decode state GB/s (256 x 96 heads, 1 token)", "value": dec_gbs,
                        "unit": "GB/s", "us_per_step": dms * 1e3,
                        "roofline": {"bound": "hbm", "achieved": dec_all_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                    "frac": dec_all_gbs / peaks["hbm_gbs"], "traffic": None,
+                                    "frac": dec_all_gbs / peaks["hbm_gbs"],
+                                    "traffic": None if DECODE_TRAFFIC_PER_HEAD is None else DECODE_TRAFFIC_PER_HEAD * H,
                                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes}},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_prefill * args.steps,
