@@ -97,12 +97,13 @@ enum {
   BAR_M1 = 3,              // K_decay S, Q_decay S done
   BAR_M2 = 4,              // U done
   BAR_M34 = 5,             // state update and O done
-  BAR_KQ = 6,              // prep -> recurrent: [K_decay; Q_decay] and a_last of the chunk written
+  BAR_KQ = 6,              // prep -> recurrent: [K_decay; Q_decay] of the chunk written
   BAR_IM = 7,              // prep -> recurrent: [INV Diag(beta); M_qk] written
   BAR_KR = 8,              // prep -> recurrent: K_restore written
   BAR_QK = 9,              // raw q, k of the chunk landed in the [K_decay; Q_decay] buffer (TMA)
   BAR_G = 10,              // g of the chunk landed in the QA/KA region (TMA)
-  kNumBars = 11
+  BAR_AL = 11,             // prep -> recurrent: a_last of the chunk written (two arrivals)
+  kNumBars = 12
 };
 enum { CTRL_TMEM = 0, CTRL_ABORT = 1, CTRL_VALID = 2 };
 
@@ -512,10 +513,16 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
           }
           break;
       }
-      if (tb == 0 && tql == 0) {
-        float4* dst = reinterpret_cast<float4*>(sm + SM_AL) + ((n & 1) * 128 + cg * 8) / 4;
-        dst[0] = make_float4(al[0], al[1], al[2], al[3]);
-        dst[1] = make_float4(al[4], al[5], al[6], al[7]);
+      if (tb == 0) {  // warps 0 and 1 (channels 0-63, 64-127) publish a_last
+        if (tql == 0) {
+          float4* dst = reinterpret_cast<float4*>(sm + SM_AL) + ((n & 1) * 128 + cg * 8) / 4;
+          dst[0] = make_float4(al[0], al[1], al[2], al[3]);
+          dst[1] = make_float4(al[4], al[5], al[6], al[7]);
+        }
+        // The recurrence reads slot n & 1 before it issues the copy of chunk n + 1's q, k,
+        // which this group waited for above: the slot is never overwritten early.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[BAR_AL]);
       }
     }
 
@@ -685,12 +692,18 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
                          i == c0 + e + 3 ? 1.f : 0.f);
       r[e] = v4.x; r[e + 1] = v4.y; r[e + 2] = v4.z; r[e + 3] = v4.w;
     }
-    tmem_st32(tmem + tl + kTS + c0, r);
     uint8_t* dst = sm + SM_S16 + (g >> 1) * 16384;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       st4(dst + sw128(i, 64 * (g & 1) + 16 * c), pack_half2(r[8 * c], r[8 * c + 1]), pack_half2(r[8 * c + 2], r[8 * c + 3]),
           pack_half2(r[8 * c + 4], r[8 * c + 5]), pack_half2(r[8 * c + 6], r[8 * c + 7]));
+    // TMEM holds the state already decayed by the first chunk's a_last (the update adds
+    // K_restore^T U to Diag(a_last) S); the fp16 operand keeps the entry state itself.
+    if (g == 0 && !mbar_wait(&bars[BAR_AL], 0)) ctrl[CTRL_ABORT] = 1;
+    const float al0 = alast[i];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) r[e] *= al0;
+    tmem_st32(tmem + tl + kTS + c0, r);
   }
   tmem_wait_st();
   if (tid == 0) {
@@ -727,20 +740,6 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
         mma_f16(tmem + kTR1, dKQ + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4), dS16 + ((kk * 2048) >> 4), id_k_mn,
                 kk > 0);
       mma_commit(&bars[BAR_M1]);
-    }
-    // ---- S <- Diag(a_last) S in TMEM (the previous update has completed)
-    {
-      const float al = alast[(n & 1) * 128 + i];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float r[32];
-        tmem_ld32(tmem + tl + kTS + g * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] *= al;
-        tmem_st32(tmem + tl + kTS + g * 32, r);
-      }
-      tmem_wait_st();
     }
     // ---- X = V - P (rows past the sequence end are zero)
     if (!mbar_wait(&bars[BAR_M1], n & 1) || !mbar_wait(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
@@ -841,8 +840,15 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
         }
       }
     }
-    // ---- state -> fp16 operand of the next chunk; checkpoint / final state in fp32
+    // ---- state -> fp16 operand of the next chunk; checkpoint / final state in fp32; the
+    //      TMEM copy is decayed by the next chunk's a_last for its update (S <- Diag(a_last) S)
     {
+      const bool next = n + 1 < n_chunks;
+      float al_next = 1.f;
+      if (next) {
+        if (!mbar_wait(&bars[BAR_AL], (n + 1) & 1)) ctrl[CTRL_ABORT] = 1;
+        al_next = alast[((n + 1) & 1) * 128 + i];
+      }
       const int pos = min((cidx + 1) * kChunk, w.len);
       float* ckdst = nullptr;
       if (ck < w.ck_end && p.ckpt_pos[ck] == pos) {
@@ -871,7 +877,13 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
 #pragma unroll
           for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
         }
+        if (next) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] *= al_next;
+          tmem_st32(tmem + tl + kTS + g * 32, r);
+        }
       }
+      tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -945,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   // ---- setup: barriers, TMEM
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], 1);
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], b == BAR_AL ? 2 : 1);
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q); tma_prefetch_desc(&p.tm_k); tma_prefetch_desc(&p.tm_v); tma_prefetch_desc(&p.tm_g);
     ctrl[CTRL_ABORT] = 0;
