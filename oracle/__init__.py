@@ -16,6 +16,9 @@ Contents
 ``segments``
     the segment algebra of "部署 Kimi K3 ..." section 2 (cumulative transition M,
     zero-start state S~, combine, entry state S = S~ + M S_in).
+``epilogue``
+    the output stage of "Kimi K3.1 Pro 架构完全拆解" section 3.3: head-wise RMSNorm of the
+    recurrent output, gated channel by channel by the sigmoid of supplied gate logits.
 """
 from __future__ import annotations
 

@@ -289,3 +289,53 @@ def pin_decode_commit():
 ALL_PINS = [pin_single_token, pin_decay_only, pin_identity_token, pin_retrieval,
             pin_orthonormal_write, pin_matrix_form, pin_linearity, pin_chunk_form,
             pin_segments, pin_restart_2560, pin_packing_and_checkpoints, pin_decode_commit]
+
+
+# ------------------------------------------------------------------ output epilogue
+# "Kimi K3.1 Pro 架构完全拆解" section 3.3: y = W_o [Sigmoid(W_g x) (.) RMSNorm(o~)], the
+# bracket computed by oracle.epilogue.gated_rmsnorm.
+def pin_epilogue_hand_values():
+    """d = 4, o = (1, -2, 2, -4): mean square 25/4, so with eps = 0 the norm is o / 2.5;
+    gate logits (0, 0, ln 3, -ln 3) give sigmoids (1/2, 1/2, 3/4, 1/4); gamma = (1, 2, 1, 4)."""
+    from oracle.epilogue import gated_rmsnorm
+    o = np.array([1.0, -2.0, 2.0, -4.0])
+    a = np.array([0.0, 0.0, np.log(3.0), -np.log(3.0)])
+    gam = np.array([1.0, 2.0, 1.0, 4.0])
+    want = np.array([0.5 * 1 * 1 / 2.5, 0.5 * 2 * -2 / 2.5, 0.75 * 1 * 2 / 2.5, 0.25 * 4 * -4 / 2.5])
+    got = gated_rmsnorm(o, a, gam, eps=0.0)
+    assert np.allclose(got, want, rtol=1e-15, atol=0), (got, want)
+
+
+def pin_epilogue_invariants():
+    """With eps = 0: scale invariance z(c o) = z(o) for c > 0, sign flip z(-o) = -z(o), unit
+    root-mean-square of the normalised row (gate logits -> +inf, gamma = 1), and a sigmoid of
+    0 halves it; eps > 0 shrinks rows with a small norm (o = 0 maps to 0)."""
+    from oracle.epilogue import gated_rmsnorm, sigmoid
+    rng = np.random.default_rng(5)
+    o = rng.standard_normal((3, 128))
+    a = rng.standard_normal((3, 128))
+    z = gated_rmsnorm(o, a, eps=0.0)
+    assert np.allclose(gated_rmsnorm(7.5 * o, a, eps=0.0), z, rtol=1e-13)
+    assert np.allclose(gated_rmsnorm(-o, a, eps=0.0), -z, rtol=1e-13)
+    big = np.full_like(o, 60.0)
+    n = gated_rmsnorm(o, big, eps=0.0)
+    assert np.allclose(np.sqrt(np.mean(n * n, axis=-1)), 1.0, rtol=1e-13)
+    h = gated_rmsnorm(o, np.zeros_like(o), eps=0.0)
+    assert np.allclose(h, 0.5 * n, rtol=1e-13)
+    assert np.all(gated_rmsnorm(np.zeros((2, 8)), np.zeros((2, 8)), eps=1e-5) == 0.0)
+    s = 1e-3 * o
+    shr = gated_rmsnorm(s, big, eps=1e-5)
+    assert np.all(np.sqrt(np.mean(shr * shr, axis=-1)) < 1.0)
+    assert np.allclose(sigmoid(np.array([-800.0, 0.0, 800.0])), [0.0, 0.5, 1.0], atol=0)
+
+
+def pin_epilogue_eps_closed_form():
+    """A constant row o = c (mean square c^2) with eps > 0 normalises to c / sqrt(c^2 + eps):
+    c = 0.01, eps = 1e-4 gives 1 / sqrt(2) (times sigmoid and gamma)."""
+    from oracle.epilogue import gated_rmsnorm
+    o = np.full(128, 0.01)
+    z = gated_rmsnorm(o, np.zeros(128), np.full(128, 2.0), eps=1e-4)
+    assert np.allclose(z, 0.5 * 2.0 / np.sqrt(2.0), rtol=1e-14), z[:4]
+
+
+ALL_PINS += [pin_epilogue_hand_values, pin_epilogue_invariants, pin_epilogue_eps_closed_form]

@@ -52,3 +52,35 @@ def test_mutant_is_caught(tmp_path, name, monkeypatch):
         except (AssertionError, oracle.OracleError):
             caught.append(pin.__name__)
     assert caught, f"mutant {name} passed every pin"
+
+
+# The output epilogue ("Kimi K3.1 Pro 架构完全拆解" section 3.3) is plain numpy: each mutant
+# is the module's source with one textual change, loaded in place of the real module.
+EPILOGUE_MUTANTS = {
+    "rms_uses_sum": ("np.mean(o * o, axis=-1, keepdims=True)", "np.sum(o * o, axis=-1, keepdims=True)"),
+    "rms_without_sqrt": ("np.sqrt(ms + eps)", "(ms + eps)"),
+    "eps_outside_sqrt": ("np.sqrt(ms + eps)", "(np.sqrt(ms) + eps)"),
+    "gate_not_sigmoid": ("return sigmoid(a) * g * o", "return a * g * o"),
+    "gamma_dropped": ("return sigmoid(a) * g * o", "return sigmoid(a) * o"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EPILOGUE_MUTANTS))
+def test_epilogue_mutant_is_caught(name, monkeypatch):
+    import sys
+    import types
+    import oracle.epilogue as real
+    old, new = EPILOGUE_MUTANTS[name]
+    src = open(real.__file__).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mod = types.ModuleType("oracle.epilogue")
+    exec(compile(src.replace(old, new), real.__file__, "exec"), mod.__dict__)
+    monkeypatch.setitem(sys.modules, "oracle.epilogue", mod)
+    caught = []
+    for pin in (oracle_pins.pin_epilogue_hand_values, oracle_pins.pin_epilogue_invariants,
+                oracle_pins.pin_epilogue_eps_closed_form):
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
