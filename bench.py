@@ -238,6 +238,31 @@ def run_ours(args, world, rank, local):
     achieved_gbs = alg_bytes / launch_s / 1e9
     achieved_tflops = alg_flop / launch_s / 1e12
 
+    # the same prefill with the fused output stage (kda_prefill_gated: head-wise RMSNorm x
+    # sigmoid gate); the gate logits add 2 d bytes per (token, head) to the algorithmic bytes
+    gate, nw = inputs.make_output_stage(T, H, seed=1, device=dev)
+
+    def gstep():
+        kda.prefill(x.q, x.k, x.v, x.g, x.beta, cu, o=o, S_out=S, workspace=ws, stream=stream, gate=gate,
+                    norm_weight=nw, eps=1e-5)
+
+    for _ in range(max(args.warmup, 3)):
+        gstep()
+    torch.cuda.synchronize(dev)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        gstep()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    gms = g0.elapsed_time(g1) / args.steps
+    g_bytes = alg_bytes + T * H * 2 * D
+    gated = {"metric": "KDA prefill + fused output stage tokens/s (H=96, d=128)", "value": T / (gms / 1e3),
+             "unit": "tokens/s", "ms_per_step": gms,
+             "roofline": {"bound": "hbm", "achieved": g_bytes / (gms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": g_bytes / (gms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                          "kernel": "prefill_kernel (gated)", "bytes_per_launch": g_bytes}}
+
     # decode: 256 sequences x 96 heads, one token; state stream against HBM
     dx = inputs.make_workload("decode", device=dev)
     Sd = dx.S0.clone()
@@ -325,6 +350,7 @@ def run_ours(args, world, rank, local):
                                     "frac": dec_all_gbs / peaks["hbm_gbs"],
                                     "traffic": None if DECODE_TRAFFIC_PER_HEAD is None else DECODE_TRAFFIC_PER_HEAD * H,
                                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes}},
+            "gated": gated,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_prefill * args.steps,
             "clocks": clk.summary(),

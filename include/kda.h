@@ -130,6 +130,32 @@ kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, 
 
 
 /*
+ * kda_prefill_gated -- kda_prefill with the layer's output stage fused into the output
+ * write: instead of o, it writes
+ *
+ *     y[t, h, :] = sigmoid(gate[t, h, :]) * norm_weight * o~ / sqrt(mean_c(o~[c]^2) + eps)
+ *
+ * where o~ = S_t^T q_t is the recurrent output kda_prefill would write (kept in fp32, not
+ * rounded, before the normalisation).  Source: "Kimi K3.1 Pro 架构完全拆解" section 3.3
+ * (full-rank output gate): y_t = W_o [Sigmoid(W_g x_t) * RMSNorm(o~_t)]; this computes the
+ * bracket, with the gate logits W_g x_t supplied by the caller.  The page names RMSNorm
+ * without its weight or epsilon: norm_weight is a per-channel weight shared by all heads
+ * and eps is added to the mean square.
+ *
+ *   gate         [total_tokens, H, d] bf16 gate logits (read only)
+ *   norm_weight  [d] fp32, or NULL for ones
+ *   eps          >= 0 and finite (else KDA_ERR_INVALID_ARG)
+ *   y            [total_tokens, H, d] bf16 (round to nearest even), in place of o
+ * Every other argument, the state outputs and the errors are those of kda_prefill.
+ */
+kda_status kda_prefill_gated(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                             const float* beta, const kda_bf16* gate, const float* norm_weight, float eps,
+                             const float* S_in, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                             const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* y,
+                             float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
+                             size_t workspace_bytes, int* dev_status, cudaStream_t stream);
+
+/*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
  *
  * This entry point has no counterpart on the pages; it exists for the library's users.

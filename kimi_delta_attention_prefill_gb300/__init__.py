@@ -4,7 +4,8 @@ Python binding of the C ABI in ``include/kda.h``: argument marshalling only.  Ev
 step of the computation runs in the CUDA kernels of ``libkda.so`` (sm_103a); there is
 no CPU or PyTorch fallback, and a missing library raises ``KdaLibraryError``.
 
-Functions mirror the C entry points: :func:`prefill` (``kda_prefill``),
+Functions mirror the C entry points: :func:`prefill` (``kda_prefill``, or
+``kda_prefill_gated`` when gate logits are given),
 :func:`decode` (``kda_decode``), :func:`prefill_workspace_size`
 (``kda_prefill_workspace_size``), :func:`status_string` (``kda_status_string``).
 Tensors are torch CUDA tensors; the launch goes to the current torch stream unless
@@ -63,6 +64,10 @@ def library():
             lib.kda_prefill.restype = _c_int
             lib.kda_prefill.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                         [_c_int, _c_int, _c_int, _vp, _c_sz, _vp, _vp])
+            lib.kda_prefill_gated.restype = _c_int
+            lib.kda_prefill_gated.argtypes = ([_vp] * 7 + [ctypes.c_float] + [_vp, _vp] + [_c_int, _c_i64] +
+                                              [_vp, _vp, _c_i64] + [_vp] * 3 +
+                                              [_c_int, _c_int, _c_int, _vp, _c_sz, _vp, _vp])
             lib.kda_prefill_noalloc.restype = _c_int
             lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                                 [_c_int, _c_int, _c_int, _vp, _vp])
@@ -135,12 +140,17 @@ def prefill_workspace_size(n_seq, H, total_tokens, n_segments=0, d=HEAD_DIM) -> 
 
 
 def prefill(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt_pos=None, o=None, S_out=None,
-            ckpts=None, n_segments=0, workspace=None, dev_status=None, stream=None):
+            ckpts=None, n_segments=0, workspace=None, dev_status=None, stream=None, gate=None,
+            norm_weight=None, eps=1e-5):
     """Chunkwise prefill over packed sequences.
 
     q, k, v ``[T, H, 128]`` bf16; g ``[T, H, 128]`` fp32; beta ``[T, H]`` fp32;
     cu_seqlens ``[N+1]`` int32 (device); S_in ``[N, H, 128, 128]`` fp32 or None;
     ckpt_off ``[N+1]`` / ckpt_pos ``[n_ckpt]`` int32 (device) or None.
+    With ``gate`` (``[T, H, 128]`` bf16 gate logits) the output stage is fused
+    (``kda_prefill_gated``): the returned ``o`` holds
+    ``sigmoid(gate) * norm_weight * o~ / sqrt(mean(o~^2) + eps)`` (``norm_weight`` ``[128]``
+    fp32 or None for ones).
     Returns ``(o, S_out, ckpts)``.
     """
     T, H, d = q.shape
@@ -173,12 +183,24 @@ def prefill(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt_pos=Non
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if dev_status is not None:
         _need(dev_status, "dev_status", torch.int32)
-    st = library().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_in), _ptr(cu_seqlens),
-                               n_seq, T, _ptr(ckpt_off), _ptr(ckpt_pos), n_ckpt, _ptr(o), _ptr(S_out),
-                               _ptr(ckpts), H, d, int(n_segments), _ptr(workspace), ws_bytes, _ptr(dev_status),
-                               _stream_handle(stream))
+    if gate is None:
+        st = library().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_in), _ptr(cu_seqlens),
+                                   n_seq, T, _ptr(ckpt_off), _ptr(ckpt_pos), n_ckpt, _ptr(o), _ptr(S_out),
+                                   _ptr(ckpts), H, d, int(n_segments), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                   _stream_handle(stream))
+        if st != 0:
+            raise KdaError(st, "kda_prefill")
+        return o, S_out, ckpts
+    _need(gate, "gate", torch.bfloat16, q.shape)
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", torch.float32, (d,))
+    st = library().kda_prefill_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(gate), _ptr(norm_weight),
+                                     float(eps), _ptr(S_in), _ptr(cu_seqlens), n_seq, T, _ptr(ckpt_off),
+                                     _ptr(ckpt_pos), n_ckpt, _ptr(o), _ptr(S_out), _ptr(ckpts), H, d,
+                                     int(n_segments), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                     _stream_handle(stream))
     if st != 0:
-        raise KdaError(st, "kda_prefill")
+        raise KdaError(st, "kda_prefill_gated")
     return o, S_out, ckpts
 
 

@@ -3,6 +3,7 @@
 // Nothing here allocates device memory or keeps per-call state; the only cached
 // values are per-device properties (compute capability, SM count).
 #include <cuda_runtime.h>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 
@@ -84,11 +85,15 @@ size_t kda_prefill_workspace_size(int n_seq, int H, int d, int64_t total_tokens,
   return kda::prefill_workspace_bytes(n_seq, H, total_tokens, n_segments, sms);
 }
 
-kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
-                       const float* S_in, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
-                       const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* o,
-                       float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
-                       size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+kda_status prefill_impl(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
+                        const kda_bf16* gate, const float* norm_weight, float eps, const float* S_in,
+                        const int32_t* cu_seqlens, int n_seq, int64_t total_tokens, const int32_t* ckpt_off,
+                        const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* o, float* S_out, float* ckpts, int H,
+                        int d, int n_segments, void* workspace, size_t workspace_bytes, int* dev_status,
+                        cudaStream_t stream) {
   if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
   if (n_seq < 0 || H < 0 || total_tokens < 0 || n_ckpt < 0 || n_segments < 0) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0x7fffffffLL || static_cast<int64_t>(n_seq) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
@@ -115,8 +120,36 @@ kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, 
   a.ckpt_pos = ckpt_pos; a.n_ckpt = n_ckpt;
   a.o = o; a.S_out = S_out; a.ckpts = ckpts; a.H = H; a.n_segments = n_segments;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = dev_status; a.stream = stream;
+  a.gate = gate; a.norm_weight = norm_weight; a.eps = eps;
   cudaError_t e = kda::launch_prefill(a, sms);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
+                       const float* S_in, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                       const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* o,
+                       float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
+                       size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  return prefill_impl(q, k, v, g, beta, nullptr, nullptr, 0.f, S_in, cu_seqlens, n_seq, total_tokens, ckpt_off,
+                      ckpt_pos, n_ckpt, o, S_out, ckpts, H, d, n_segments, workspace, workspace_bytes, dev_status,
+                      stream);
+}
+
+kda_status kda_prefill_gated(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                             const float* beta, const kda_bf16* gate, const float* norm_weight, float eps,
+                             const float* S_in, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                             const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* y,
+                             float* S_out, float* ckpts, int H, int d, int n_segments, void* workspace,
+                             size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0 && n_seq > 0 && H > 0 && !gate) return KDA_ERR_INVALID_ARG;
+  if (!aligned(gate, 16) || !aligned(norm_weight, 16)) return KDA_ERR_ALIGNMENT;
+  return prefill_impl(q, k, v, g, beta, gate, norm_weight, eps, S_in, cu_seqlens, n_seq, total_tokens, ckpt_off,
+                      ckpt_pos, n_ckpt, y, S_out, ckpts, H, d, n_segments, workspace, workspace_bytes, dev_status,
+                      stream);
 }
 
 }  // extern "C"

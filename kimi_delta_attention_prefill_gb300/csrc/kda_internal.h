@@ -34,6 +34,10 @@ struct PrefillArgs {
   const int32_t* ckpt_pos;
   int64_t n_ckpt;
   void* o;
+  // output stage (kda_prefill_gated): gate logits [T, H, d] bf16 or nullptr for plain o
+  const void* gate = nullptr;
+  const float* norm_weight = nullptr;  // [d] or nullptr for ones
+  float eps = 0.f;
   float* S_out;
   float* ckpts;
   int H;

@@ -54,7 +54,7 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kRThreads = 128;  // recurrent group: warps 0-3 (TMEM lane quarters 0-3)
 constexpr int kPThreads = 256;  // prep group: warps 4-11
-constexpr uint32_t kBarR = 1, kBarP = 2;  // named barrier ids
+constexpr uint32_t kBarR = 1, kBarP = 2, kBarXU = 3;  // named barrier ids (kBarXU: recurrent warps 0-1)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Block totals table: [4 blocks][16 channel groups], 12 floats per group (8 used), so the
@@ -65,7 +65,8 @@ constexpr int kTotCg = 12, kTotPitch = 16 * kTotCg;
 //   TS  [0, 128)   the state S, fp32 (lane = d_k row)
 //   TR1 [128, 256) lanes 0-63: P = K_decay S, then U; lanes 64-127: Q_decay S, then O
 //   TLM [256, 416) lanes 0-63: M_qk rows, lanes 64-127: L rows, 160 columns (4 blocks)
-constexpr uint32_t kTS = 0, kTR1 = 128, kTLM = 256;
+//   TF  [416, 480) lanes 64-127: output-stage factors sigmoid(a) w, packed half2 (recurrent)
+constexpr uint32_t kTS = 0, kTR1 = 128, kTLM = 256, kTF = 416;
 __host__ __device__ constexpr uint32_t lm_col(int tb) { return tb == 0 ? 0u : tb == 1 ? 16u : tb == 2 ? 48u : 96u; }
 
 // Shared memory (bytes from a 1024-aligned base).
@@ -128,6 +129,9 @@ struct KParams {
   const int32_t* ckpt_off;
   const int32_t* ckpt_pos;
   __nv_bfloat16* o;
+  const __nv_bfloat16* gate;  // output stage: gate logits [T, H, d], or nullptr for plain o
+  const float* norm_weight;   // output stage: [d] per-channel weight, or nullptr (ones)
+  float eps;
   float* S_out;
   float* ckpts;
   int* status;
@@ -608,7 +612,6 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       for (int gi = gb; gi < ge; ++gi) {
         float r[16];
         tmem_ld16(tmem + tl + kTLM + (g0 + gi) * 16, r);
-        tmem_wait_ld();
         const int col = (g0 + gi) * 16;
         if (col < lo || col >= hi) continue;
         const int s0 = col - lo;
@@ -678,6 +681,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   const uint32_t id_mn_mn = idesc_f16(128, 128, false, true, true);
   const float* alast = reinterpret_cast<const float*>(sm + SM_AL);
   const int i = tid;  // state row owned by this thread
+  const bool gated = p.gate != nullptr && do_o;  // output stage on the o rows
 
   // entry state -> TMEM (fp32) and the fp16 operand copy
 #pragma unroll
@@ -724,6 +728,14 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
     const int valid = min(kChunk, w.len - cidx * kChunk);
     const int vs = n & 1;
+    // the output stage's gate-logit rows of the next chunk, pulled into L2 a chunk ahead
+    if (gated && rw >= 2 && n + 1 < n_chunks && kChunk + tid - 64 < w.len - cidx * kChunk) {
+      const char* ar =
+          reinterpret_cast<const char*>(p.gate + ((row0 + kChunk + tid - 64) * p.H + w.h) * kHeadDim);
+      prefetch_l2(ar);
+      prefetch_l2(ar + 128);
+      prefetch_l2(ar + 255);
+    }
     if (tid == 0 && n >= 1 && n + 1 < n_chunks) {  // stage vs ^ 1 was consumed by the previous chunk's X
       mbar_arrive_expect_tx(&bars[BAR_V0 + (vs ^ 1)], 16384);
       const int r0 = static_cast<int>(row0 + kChunk);
@@ -742,87 +754,120 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       mma_commit(&bars[BAR_M1]);
     }
     // ---- X = V - P (rows past the sequence end are zero)
-    if (!mbar_wait(&bars[BAR_M1], n & 1) || !mbar_wait(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
-    tc_fence_after();
-    if (tid == 0 && n + 1 < n_chunks) issue_qk(p, w, sm, bars, cidx + 1);  // the buffer is free again
+    //      Warps 0-1 own rows 0-63 (P, X, U); warps 2-3 meanwhile prepare the output stage.
     if (rw < 2) {
-      const int t = tid;
-      const bool mk = t < valid;
-      const uint8_t* vt = sm + SM_V + vs * 16384;
+      if (!mbar_wait(&bars[BAR_M1], n & 1) || !mbar_wait(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
+      tc_fence_after();
+      if (tid == 0 && n + 1 < n_chunks) issue_qk(p, w, sm, bars, cidx + 1);  // the buffer is free again
+      {
+        const int t = tid;
+        const bool mk = t < valid;
+        const uint8_t* vt = sm + SM_V + vs * 16384;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float r[32];
-        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
-        tmem_wait_ld();
-        const uint8_t* vp = vt + (g >> 1) * 8192;
-        uint8_t* xp = sm + SM_XU + (g >> 1) * 8192;
+        for (int g = 0; g < 4; ++g) {
+          float r[32];
+          tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+          const uint8_t* vp = vt + (g >> 1) * 8192;
+          uint8_t* xp = sm + SM_XU + (g >> 1) * 8192;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float vv[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vp + sw128(t, 64 * (g & 1) + 16 * c)), vv);
-          float x[8];
+          for (int c = 0; c < 4; ++c) {
+            float vv[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(vp + sw128(t, 64 * (g & 1) + 16 * c)), vv);
+            float x[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = mk ? (v_zero ? 0.f : vv[e]) - r[8 * c + e] : 0.f;
-          st4(xp + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]),
-              pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+            for (int e = 0; e < 8; ++e) x[e] = mk ? (v_zero ? 0.f : vv[e]) - r[8 * c + e] : 0.f;
+            st4(xp + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]),
+                pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+          }
         }
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    named_bar_sync(kBarR, kRThreads);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(kBarXU, 64);
 
-    // ---- U = INV Diag(beta) X (lanes 64-127 keep Q_decay S)
-    if (tid == 0) {
-      if (!mbar_wait(&bars[BAR_IM], n & 1)) ctrl[CTRL_ABORT] = 1;
+      // ---- U = INV Diag(beta) X (lanes 64-127 keep Q_decay S)
+      if (tid == 0) {
+        if (!mbar_wait(&bars[BAR_IM], n & 1)) ctrl[CTRL_ABORT] = 1;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), dXU + ((kk * 2048) >> 4), id_k_mn, kk > 0, 0u, 0u,
+                         0xffffffffu, 0xffffffffu);
+        mma_commit(&bars[BAR_M2]);
+      }
+      if (!mbar_wait(&bars[BAR_M2], n & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
+      {
+        const int t = tid;
+        const bool mk = t < valid;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), dXU + ((kk * 2048) >> 4), id_k_mn, kk > 0, 0u, 0u,
-                       0xffffffffu, 0xffffffffu);
-      mma_commit(&bars[BAR_M2]);
-    }
-    if (!mbar_wait(&bars[BAR_M2], n & 1)) ctrl[CTRL_ABORT] = 1;
-    tc_fence_after();
-    if (rw < 2) {
-      const int t = tid;
-      const bool mk = t < valid;
+        for (int g = 0; g < 4; ++g) {
+          float r[32];
+          tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+          uint8_t* up = sm + SM_XU + (g >> 1) * 8192;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float r[32];
-        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
-        tmem_wait_ld();
-        uint8_t* up = sm + SM_XU + (g >> 1) * 8192;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float* x = r + 8 * c;
-          st4(up + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(mk ? x[0] : 0.f, mk ? x[1] : 0.f),
-              pack_half2(mk ? x[2] : 0.f, mk ? x[3] : 0.f), pack_half2(mk ? x[4] : 0.f, mk ? x[5] : 0.f),
-              pack_half2(mk ? x[6] : 0.f, mk ? x[7] : 0.f));
+          for (int c = 0; c < 4; ++c) {
+            const float* x = r + 8 * c;
+            st4(up + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(mk ? x[0] : 0.f, mk ? x[1] : 0.f),
+                pack_half2(mk ? x[2] : 0.f, mk ? x[3] : 0.f), pack_half2(mk ? x[4] : 0.f, mk ? x[5] : 0.f),
+                pack_half2(mk ? x[6] : 0.f, mk ? x[7] : 0.f));
+          }
         }
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    named_bar_sync(kBarR, kRThreads);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(kBarXU, 64);
 
-    // ---- S += K_restore^T U ; O += M_qk U (lanes 0-63 untouched)
-    if (tid == 0) {
-      if (!mbar_wait(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
-      tc_fence_after();
+      // ---- S += K_restore^T U ; O += M_qk U (lanes 0-63 untouched)
+      if (tid == 0) {
+        if (!mbar_wait(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
+        tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ud = dXU + ((kk * 2048) >> 4);
-        mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_mn_mn, 1);
-        if (do_o)
-          mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), ud, id_k_mn, 1, 0xffffffffu, 0xffffffffu, 0u, 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ud = dXU + ((kk * 2048) >> 4);
+          mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_mn_mn, 1);
+          if (do_o)
+            mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), ud, id_k_mn, 1, 0xffffffffu, 0xffffffffu, 0u, 0u);
+        }
+        mma_commit(&bars[BAR_M34]);
       }
-      mma_commit(&bars[BAR_M34]);
+    } else if (gated) {
+      // output-stage factors f = sigmoid(a) w of row t, 32 per step, into TF (half2 pairs)
+      const int t = tid - 64;
+      const bool wr = t < valid;
+      const uint4* arow = reinterpret_cast<const uint4*>(p.gate + ((row0 + t) * p.H + w.h) * kHeadDim);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 a4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a4[c] = wr ? __ldg(arow + 4 * q4 + c) : make_uint4(0, 0, 0, 0);
+        float f[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float a[8];
+          bf16x8_to_f32(a4[c], a);
+          float wv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+          if (p.norm_weight) {
+            const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.norm_weight + 32 * q4 + 8 * c));
+            const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.norm_weight + 32 * q4 + 8 * c + 4));
+            wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+            wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+          }
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)  // sigmoid(a) = 1 / (1 + 2^(-a log2 e))
+            y[e] = wv[e] * __fdividef(1.f, 1.f + exp2_fast(-a[e] * kLog2e));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[4 * c + e] = __uint_as_float(pack_half2(y[2 * e], y[2 * e + 1]));
+        }
+        tmem_st16(tmem + tl + kTF + 16 * q4, f);
+      }
+      tmem_wait_st();
     }
     if (!mbar_wait(&bars[BAR_M34], n & 1)) ctrl[CTRL_ABORT] = 1;
     tc_fence_after();
     // ---- outputs (rows in lanes 64-127)
-    if (do_o && rw >= 2) {
+    if (do_o && rw >= 2 && !gated) {
       const int t = tid - 64;
       const bool wr = t < valid;
       __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim;
@@ -830,13 +875,51 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       for (int g = 0; g < 4; ++g) {
         float r[32];
         tmem_ld32(tmem + tl + kTR1 + g * 32, r);
-        tmem_wait_ld();
         if (wr) {
           uint4* dst = reinterpret_cast<uint4*>(orow + g * 32);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             dst[c] = make_uint4(pack_bf162(r[8 * c], r[8 * c + 1]), pack_bf162(r[8 * c + 2], r[8 * c + 3]),
                                 pack_bf162(r[8 * c + 4], r[8 * c + 5]), pack_bf162(r[8 * c + 6], r[8 * c + 7]));
+        }
+      }
+    }
+    // ---- output stage: row t of o~ is normalised by its root mean square and gated,
+    //      y = sigmoid(a) w o~ / sqrt(mean(o~^2) + eps) ("Kimi K3.1 Pro 架构完全拆解" 3.3).
+    //      A thread owns a whole row: one TMEM pass for the sum of squares, a second for y
+    //      with the factors sigmoid(a) w that warps 2-3 left in TF while rows 0-63 ran.
+    if (do_o && rw >= 2 && gated) {
+      const int t = tid - 64;
+      const bool wr = t < valid;
+      __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim;
+      float ss = 0.f;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ss = fmaf(r[e], r[e], ss);
+      }
+      const float scale = rsqrtf(ss * (1.f / kHeadDim) + p.eps);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32], f[16];
+        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+        tmem_ld16(tmem + tl + kTF + g * 16, f);
+        if (wr) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + g * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&f[4 * c + e]));
+              y[2 * e] = r[8 * c + 2 * e] * scale * ff.x;
+              y[2 * e + 1] = r[8 * c + 2 * e + 1] * scale * ff.y;
+            }
+            dst[c] = make_uint4(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]), pack_bf162(y[4], y[5]),
+                                pack_bf162(y[6], y[7]));
+          }
         }
       }
     }
@@ -860,7 +943,6 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       for (int g = 0; g < 4; ++g) {
         float r[32];
         tmem_ld32(tmem + tl + kTS + g * 32, r);
-        tmem_wait_ld();
         uint8_t* dst = sm + SM_S16 + (g >> 1) * 16384;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -1034,6 +1116,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.q = static_cast<const __nv_bfloat16*>(a.q); p.k = static_cast<const __nv_bfloat16*>(a.k); p.g = a.g;
   p.beta = a.beta; p.S_in = a.S_in; p.cu = a.cu_seqlens; p.ckpt_off = a.ckpt_off; p.ckpt_pos = a.ckpt_pos;
   p.o = static_cast<__nv_bfloat16*>(a.o); p.S_out = a.S_out; p.ckpts = a.ckpts; p.status = a.status;
+  p.gate = static_cast<const __nv_bfloat16*>(a.gate); p.norm_weight = a.norm_weight; p.eps = a.eps;
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
   static bool attr_set = false;
   if (!attr_set) {

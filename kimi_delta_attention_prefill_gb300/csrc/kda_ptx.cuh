@@ -95,6 +95,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1
                : "memory");
 }
 
+// Pull the cache line holding `ptr` into L2 (no register result, no completion tracking).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.L2 [%0];\n" ::"l"(reinterpret_cast<uint64_t>(ptr)));
+}
+
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
@@ -178,10 +183,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // 32 lanes x 32 bit, 16 consecutive columns: thread t of the warp reads lane
 // (lane base + t).  The warp may only address its own 32-lane quarter.
+// The load and its tcgen05.wait::ld are one asm statement: the destination registers are
+// only valid after the wait, and as separate statements the compiler may schedule
+// arithmetic on those registers between the two (it sees them defined by the load).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
   uint32_t* u = reinterpret_cast<uint32_t*>(r);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
       : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
         "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
       : "r"(taddr));
@@ -195,12 +204,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) 
       "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
       : "memory");
 }
-// 32 lanes x 32 bit, 32 consecutive columns.
+// 32 lanes x 32 bit, 32 consecutive columns (load and wait in one statement, as above).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
   uint32_t* u = reinterpret_cast<uint32_t*>(r);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
       : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
         "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
         "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]),

@@ -22,6 +22,10 @@ The -5 floor is the bounded log-decay of "Kimi K3.1 Pro 架构完全拆解" sect
 
 Packed (varlen) inputs draw each sequence from its own generator seeded
 ``1000 * seed + i``, so one sequence can be regenerated alone.
+
+Output stage ("Kimi K3.1 Pro 架构完全拆解" section 3.3): gate logits [T_tot, H, d] bf16
+~ N(0, 1) (the projection W_g x of a unit-scale input) and a RMSNorm weight [d] float32
+~ 1 + 0.1 N(0, 1), from their own generator (``make_output_stage``).
 """
 from __future__ import annotations
 
@@ -129,6 +133,15 @@ def make_prefill(lengths, H, d=128, seed=0, device="cpu", decay="sigmoid", s0_st
     return PrefillInputs(q, k, v, g, beta, S0, cu, off, pos,
                          meta=dict(lengths=lengths, H=H, d=d, seed=seed, decay=decay,
                                    s0_std=s0_std, ckpt_every=ckpt_every, device=str(device)))
+
+
+def make_output_stage(T, H, d=128, seed=0, device="cpu"):
+    """Gate logits ``[T, H, d]`` bf16 and RMSNorm weight ``[d]`` float32 for the fused output
+    stage, from a generator seeded ``7919 + seed`` (independent of the token draws)."""
+    gen = _gen(device, 7919 + seed)
+    gate = torch.randn((T, H, d), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    weight = 1.0 + 0.1 * torch.randn((d,), generator=gen, device=device, dtype=torch.float32)
+    return gate, weight
 
 
 def varlen_lengths(n_seq, lo, hi, seed):

@@ -105,6 +105,28 @@ def test_prefill_host_validation(lib):
         assert _prefill(lib) in (CUDA, UNSUPPORTED)
 
 
+def _prefill_gated(lib, gate=0x1700, nw=None, eps=1e-5, q=0x1000, d=128, T=64):
+    return lib.kda_prefill_gated(P(q), P(0x1100), P(0x1200), P(0x1300), P(0x1400), P(gate) if gate else None,
+                                 P(nw) if nw else None, eps, None, P(0x9000), 1, T, None, None, 0, P(0x1500),
+                                 P(0x1600), None, 2, d, 0, None, 0, None, None)
+
+
+def test_prefill_gated_host_validation(lib):
+    """The fused output stage ("Kimi K3.1 Pro 架构完全拆解" 3.3): bad eps, a missing or
+    misaligned gate / weight are rejected before any CUDA call; the rest is kda_prefill's."""
+    assert _prefill_gated(lib, eps=-1e-6) == INVALID
+    assert _prefill_gated(lib, eps=float("nan")) == INVALID
+    assert _prefill_gated(lib, eps=float("inf")) == INVALID
+    assert _prefill_gated(lib, gate=0) == INVALID
+    assert _prefill_gated(lib, gate=0x1708) == ALIGNMENT
+    assert _prefill_gated(lib, nw=0x1804) == ALIGNMENT
+    assert _prefill_gated(lib, d=64) == UNSUPPORTED
+    assert _prefill_gated(lib, q=0) == INVALID
+    if not HAS_GPU:
+        assert _prefill_gated(lib) in (CUDA, UNSUPPORTED)
+        assert _prefill_gated(lib, nw=0x1800, eps=0.0) in (CUDA, UNSUPPORTED)
+
+
 def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(4, 1, 2, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
