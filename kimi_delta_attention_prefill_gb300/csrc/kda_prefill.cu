@@ -663,6 +663,40 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
   }
 }
 
+// ------------------------------------------------------------- output stage
+// f = w sigmoid(a) for the 8 bf16 logits of `a8` and their weights, as 4 half2 pairs,
+// with one MUFU operation per pair:
+//   e = 2^(-|a| log2 e), in (0, 1]: the exponent is formed in fp32, rounded to fp16 and
+//       raised by ex2.approx.f16x2 (no overflow: the exponent is never positive);
+//   r = 1 / (1 + e), d = 1 + e in [1, 2]: the linear start 24/17 - 8/17 d (relative error
+//       at most 1/17) and two Newton steps r <- r + r (1 - d r) (error 1/17 -> 3.5e-3 ->
+//       1.2e-5, below fp16's 2^-11), in half2 fused multiply-adds;
+//   sigmoid(a) = r for a >= 0 and e r = 1 - r for a < 0 (no cancellation either way).
+__device__ __forceinline__ void sigmoid_w_half2(const uint4& a8, const uint32_t (&w2)[4], uint32_t (&f)[4]) {
+  const uint32_t u[4] = {a8.x, a8.y, a8.z, a8.w};
+  const __half2 one = __float2half2_rn(1.f);
+  const __half2 c0 = __float2half2_rn(24.f / 17.f), c1 = __float2half2_rn(-8.f / 17.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __uint_as_float(u[j] << 16), hi = __uint_as_float(u[j] & 0xffff0000u);
+    const __half2 x = __floats2half2_rn(fabsf(lo) * -kLog2e, fabsf(hi) * -kLog2e);
+    uint32_t eb;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(eb) : "r"(*reinterpret_cast<const uint32_t*>(&x)));
+    const __half2 e = *reinterpret_cast<const __half2*>(&eb);
+    const __half2 d = __hadd2(e, one);
+    __half2 r = __hfma2(d, c1, c0);
+    r = __hfma2(r, __hfma2(__hneg2(d), r, one), r);
+    r = __hfma2(r, __hfma2(__hneg2(d), r, one), r);
+    // numerator: e in the halves whose logit is negative, 1 elsewhere (sign bytes replicated)
+    uint32_t neg;
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(neg) : "r"(u[j]));
+    const uint32_t nb = (eb & neg) | (0x3C003C00u & ~neg);
+    const __half2 sg = __hmul2(*reinterpret_cast<const __half2*>(&nb), r);
+    const __half2 fw = __hmul2(sg, *reinterpret_cast<const __half2*>(&w2[j]));
+    f[j] = *reinterpret_cast<const uint32_t*>(&fw);
+  }
+}
+
 // ------------------------------------------------------------- recurrent group
 // 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (P, then U)
 // belong to warps 0-1, rows 64-127 (Q_decay S, then O) to warps 2-3; the state TS uses
@@ -836,29 +870,23 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       const int t = tid - 64;
       const bool wr = t < valid;
       const uint4* arow = reinterpret_cast<const uint4*>(p.gate + ((row0 + t) * p.H + w.h) * kHeadDim);
-#pragma unroll
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 a4[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) a4[c] = wr ? __ldg(arow + 4 * q4 + c) : make_uint4(0, 0, 0, 0);
         float f[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float a[8];
-          bf16x8_to_f32(a4[c], a);
-          float wv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+          uint32_t w2[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};  // ones
           if (p.norm_weight) {
             const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.norm_weight + 32 * q4 + 8 * c));
             const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.norm_weight + 32 * q4 + 8 * c + 4));
-            wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-            wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+            w2[0] = pack_half2(w0.x, w0.y); w2[1] = pack_half2(w0.z, w0.w);
+            w2[2] = pack_half2(w1.x, w1.y); w2[3] = pack_half2(w1.z, w1.w);
           }
-          float y[8];
+          const uint4 a8 = wr ? __ldg(arow + 4 * q4 + c) : make_uint4(0, 0, 0, 0);
+          uint32_t fc[4];
+          sigmoid_w_half2(a8, w2, fc);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)  // sigmoid(a) = 1 / (1 + 2^(-a log2 e))
-            y[e] = wv[e] * __fdividef(1.f, 1.f + exp2_fast(-a[e] * kLog2e));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) f[4 * c + e] = __uint_as_float(pack_half2(y[2 * e], y[2 * e + 1]));
+          for (int e = 0; e < 4; ++e) f[4 * c + e] = __uint_as_float(fc[e]);
         }
         tmem_st16(tmem + tl + kTF + 16 * q4, f);
       }
