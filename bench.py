@@ -45,7 +45,8 @@ CPU_SAMPLE_TOKENS = 8192  # the whole workload: about 1.5 s on 16 host cores (ab
 # (both kernels' traffic grows in proportion to the heads); the capture and the command
 # that made it are summarised in profiles/.  Set to None when the kernel changes until it is
 # captured again.
-PREFILL_TRAFFIC_PER_HEAD = 190_091_776 // 16  # bytes per head of the 8192-token launch
+PREFILL_TRAFFIC_PER_HEAD = 189_775_360 // 16  # bytes per head of the 8192-token launch
+GATED_TRAFFIC_PER_HEAD = 225_331_200 // 16  # the same launch with the fused output stage
 DECODE_TRAFFIC_PER_HEAD = 488_329_216 // 16  # bytes per head of the 256-sequence launch
 
 
@@ -260,7 +261,8 @@ def run_ours(args, world, rank, local):
     gated = {"metric": "KDA prefill + fused output stage tokens/s (H=96, d=128)", "value": T / (gms / 1e3),
              "unit": "tokens/s", "ms_per_step": gms,
              "roofline": {"bound": "hbm", "achieved": g_bytes / (gms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                          "unit": "GB/s", "frac": g_bytes / (gms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                          "unit": "GB/s", "frac": g_bytes / (gms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                          "traffic": None if GATED_TRAFFIC_PER_HEAD is None else GATED_TRAFFIC_PER_HEAD * H,
                           "kernel": "prefill_kernel (gated)", "bytes_per_launch": g_bytes}}
 
     # decode: 256 sequences x 96 heads, one token; state stream against HBM

@@ -1,6 +1,7 @@
 """Run one workload through the library a few times (for profilers and quick checks).
 
     python -m kimi_delta_attention_prefill_gb300.run_case --workload prefill_8k --heads 16 --iters 3
+    python -m kimi_delta_attention_prefill_gb300.run_case --workload prefill_8k --gated   # + output stage
 
 Prints the mean CUDA-event time per call; exits non-zero if the library reports an error.
 """
@@ -21,6 +22,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=None, help="override the length of a single-sequence prefill")
     ap.add_argument("--segments", type=int, default=0, help="prefill segment count (0 = library's choice)")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--gated", action="store_true", help="prefill with the fused output stage")
     args = ap.parse_args()
     over = {}
     if args.heads:
@@ -38,8 +40,12 @@ def main():
         off = None if x.ckpt_off is None else x.ckpt_off.cuda()
         pos = None if x.ckpt_pos is None else x.ckpt_pos.cuda()
         S0 = x.S0
+        kw = {}
+        if args.gated:
+            gate, w = inputs.make_output_stage(x.q.shape[0], x.q.shape[1], device="cuda")
+            kw = dict(gate=gate, norm_weight=w)
         run = lambda: kda.prefill(x.q, x.k, x.v, x.g, x.beta, cu, S_in=S0, ckpt_off=off, ckpt_pos=pos,
-                                  n_segments=args.segments, dev_status=status)
+                                  n_segments=args.segments, dev_status=status, **kw)
     run()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
