@@ -156,6 +156,69 @@ kda_status kda_prefill_gated(const kda_bf16* q, const kda_bf16* k, const kda_bf1
                              size_t workspace_bytes, int* dev_status, cudaStream_t stream);
 
 /*
+ * Paged state.  "部署 Kimi K3：从 KDA Kernel 到 Fleet 调度的推理 Infra 全景" section 3: the
+ * prefix cache keeps each head's state as one 64 KiB block, snapshots it at hash-aligned
+ * positions, and a hit resumes from the cached snapshot, which other requests may share;
+ * "Kimi K3.1 Pro 架构完全拆解" section 8: the states live in one unified pool.  The paged
+ * entry points address every state through such a pool:
+ *
+ *   state_pool   [n_pages, d, d] fp32, 16-byte aligned: page p holds one head's state
+ *                (row = d_k), n_pages <= 2^31 - 1
+ *   page tables  device int32; an entry is a page index in [0, n_pages) or -1 = none (a
+ *                zero entry state, or nothing written).  Another value is a device error
+ *                (KDA_ERR_DEVICE_CHECK).
+ *
+ * Copy on hit: a call writes each page at most once and never writes a page that it reads,
+ * except that a unit (one sequence and head) may write its final or committed state back
+ * to its own entry page (in place).  Before the work runs, the library checks this over
+ * the tables on the device, with an owner table in the caller's workspace (4 bytes per
+ * page): on a violation it reports KDA_ERR_DEVICE_CHECK and the call writes nothing (no
+ * outputs, no states).  A shared snapshot therefore stays bit-unchanged: a continuation
+ * names it as its entry page and a fresh page for its result.
+ */
+
+/*
+ * kda_prefill_paged -- kda_prefill / kda_prefill_gated with the states in a page pool.
+ *
+ *   s_in_page    [n_seq * H] (entry seq * H + h): page of the entry state, -1 = zeros;
+ *                NULL = all zeros
+ *   s_out_page   [n_seq * H]: page receiving the final state, -1 = not written; NULL = none
+ *   ckpt_page    [n_ckpt * H] (entry j * H + h, j in ckpt_pos order): page receiving
+ *                checkpoint j of head h, -1 = not written; required when n_ckpt > 0
+ *   gate         NULL: write o as kda_prefill does; otherwise gate / norm_weight / eps and
+ *                the output y are those of kda_prefill_gated
+ *   workspace    kda_prefill_paged_workspace_size(...) bytes, 256-byte aligned (never 0:
+ *                the page check always runs)
+ * Every other argument, the checkpoint positions and the errors are those of kda_prefill.
+ */
+size_t kda_prefill_paged_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int n_segments,
+                                        int64_t n_pages);
+kda_status kda_prefill_paged(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                             const float* beta, const kda_bf16* gate, const float* norm_weight, float eps,
+                             float* state_pool, int64_t n_pages, const int32_t* s_in_page,
+                             const int32_t* s_out_page, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                             const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt,
+                             const int32_t* ckpt_page, kda_bf16* o, int H, int d, int n_segments, void* workspace,
+                             size_t workspace_bytes, int* dev_status, cudaStream_t stream);
+
+/*
+ * kda_decode_paged -- kda_decode with the states in a page pool.
+ *
+ *   s_in_page    [B * H] (entry b * H + h): page the state is read from, -1 = zeros
+ *   s_out_page   [B * H]: page receiving the state after n_commit[b] tokens, -1 = not
+ *                written; NULL = in place (s_in_page).  A destination other than the
+ *                source always receives it, the entry state itself when n_commit[b] = 0
+ *                (speculative decode from a shared snapshot: the snapshot stays unchanged).
+ *   workspace    kda_decode_paged_workspace_size(n_pages) bytes, 256-byte aligned
+ * Every other argument and the errors are those of kda_decode.
+ */
+size_t kda_decode_paged_workspace_size(int64_t n_pages);
+kda_status kda_decode_paged(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                            const float* beta, float* state_pool, int64_t n_pages, const int32_t* s_in_page,
+                            const int32_t* s_out_page, const int32_t* n_commit, float* o, int B, int n_tok, int H,
+                            int d, void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream);
+
+/*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
  *
  * This entry point has no counterpart on the pages; it exists for the library's users.

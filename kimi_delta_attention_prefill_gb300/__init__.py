@@ -68,6 +68,17 @@ def library():
             lib.kda_prefill_gated.argtypes = ([_vp] * 7 + [ctypes.c_float] + [_vp, _vp] + [_c_int, _c_i64] +
                                               [_vp, _vp, _c_i64] + [_vp] * 3 +
                                               [_c_int, _c_int, _c_int, _vp, _c_sz, _vp, _vp])
+            lib.kda_prefill_paged_workspace_size.restype = _c_sz
+            lib.kda_prefill_paged_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_i64]
+            lib.kda_prefill_paged.restype = _c_int
+            lib.kda_prefill_paged.argtypes = ([_vp] * 7 + [ctypes.c_float] + [_vp, _c_i64, _vp, _vp, _vp] +
+                                              [_c_int, _c_i64, _vp, _vp, _c_i64, _vp, _vp] +
+                                              [_c_int, _c_int, _c_int, _vp, _c_sz, _vp, _vp])
+            lib.kda_decode_paged_workspace_size.restype = _c_sz
+            lib.kda_decode_paged_workspace_size.argtypes = [_c_i64]
+            lib.kda_decode_paged.restype = _c_int
+            lib.kda_decode_paged.argtypes = ([_vp] * 6 + [_c_i64] + [_vp] * 4 + [_c_int] * 4 +
+                                             [_vp, _c_sz, _vp, _vp])
             lib.kda_prefill_noalloc.restype = _c_int
             lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                                 [_c_int, _c_int, _c_int, _vp, _vp])
@@ -202,6 +213,114 @@ def prefill(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt_pos=Non
     if st != 0:
         raise KdaError(st, "kda_prefill_gated")
     return o, S_out, ckpts
+
+
+def _pool(state_pool, d):
+    _need(state_pool, "state_pool", torch.float32)
+    if state_pool.dim() != 3 or tuple(state_pool.shape[1:]) != (d, d):
+        raise ValueError(f"state_pool must have shape [n_pages, {d}, {d}], got {tuple(state_pool.shape)}")
+    return state_pool.shape[0]
+
+
+def _table(t, name, n):
+    if t is not None:
+        _need(t, name, torch.int32, (n,))
+    return t
+
+
+def prefill_paged_workspace_size(n_seq, H, total_tokens, n_pages, n_segments=0, d=HEAD_DIM) -> int:
+    return int(library().kda_prefill_paged_workspace_size(int(n_seq), int(H), int(d), int(total_tokens),
+                                                          int(n_segments), int(n_pages)))
+
+
+def prefill_paged(q, k, v, g, beta, cu_seqlens, state_pool, s_in_page=None, s_out_page=None, ckpt_off=None,
+                  ckpt_pos=None, ckpt_page=None, o=None, n_segments=0, workspace=None, dev_status=None,
+                  stream=None, gate=None, norm_weight=None, eps=1e-5):
+    """:func:`prefill` with every state in a page pool (``kda_prefill_paged``).
+
+    state_pool ``[n_pages, 128, 128]`` fp32; s_in_page / s_out_page ``[N * H]`` int32
+    (entry ``seq * H + h``; -1 = zeros / not written; None = all zeros / none); ckpt_page
+    ``[n_ckpt * H]`` int32 (entry ``j * H + h``).  A call never writes a page it reads
+    (except a unit's own final state in place) and writes each page once; a violation
+    writes nothing and sets ``dev_status`` to KDA_ERR_DEVICE_CHECK.  Returns ``o``.
+    """
+    T, H, d = q.shape
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape)
+    _need(beta, "beta", torch.float32, (T, H))
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seq = cu_seqlens.shape[0] - 1
+    n_pages = _pool(state_pool, d)
+    _table(s_in_page, "s_in_page", n_seq * H)
+    _table(s_out_page, "s_out_page", n_seq * H)
+    n_ckpt = 0
+    if ckpt_off is not None:
+        _need(ckpt_off, "ckpt_off", torch.int32, (n_seq + 1,))
+        _need(ckpt_pos, "ckpt_pos", torch.int32)
+        n_ckpt = ckpt_pos.shape[0]
+        _table(ckpt_page, "ckpt_page", n_ckpt * H)
+    if o is None:
+        o = torch.empty((T, H, d), dtype=torch.bfloat16, device=q.device)
+    _need(o, "o", torch.bfloat16, (T, H, d))
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, q.shape)
+        if norm_weight is not None:
+            _need(norm_weight, "norm_weight", torch.float32, (d,))
+    if workspace is None:
+        need = prefill_paged_workspace_size(n_seq, H, T, n_pages, n_segments, d)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(gate), _ptr(norm_weight),
+                                     float(eps), _ptr(state_pool), n_pages, _ptr(s_in_page), _ptr(s_out_page),
+                                     _ptr(cu_seqlens), n_seq, T, _ptr(ckpt_off), _ptr(ckpt_pos), n_ckpt,
+                                     _ptr(ckpt_page), _ptr(o), H, d, int(n_segments), _ptr(workspace), ws_bytes,
+                                     _ptr(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_prefill_paged")
+    return o
+
+
+def decode_paged_workspace_size(n_pages) -> int:
+    return int(library().kda_decode_paged_workspace_size(int(n_pages)))
+
+
+def decode_paged(q, k, v, g, beta, state_pool, s_in_page, s_out_page=None, n_commit=None, o=None, workspace=None,
+                 dev_status=None, stream=None):
+    """:func:`decode` with the states in a page pool (``kda_decode_paged``).
+
+    s_in_page ``[B * H]`` int32 (entry ``b * H + h``; -1 = a zero state); s_out_page the
+    same, or None to update in place.  A destination other than the source receives the
+    state after ``n_commit[b]`` tokens (the entry state when that is 0).  Returns ``o``.
+    """
+    B, n_tok, H, d = q.shape
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape)
+    _need(beta, "beta", torch.float32, (B, n_tok, H))
+    n_pages = _pool(state_pool, d)
+    _need(s_in_page, "s_in_page", torch.int32, (B * H,))
+    _table(s_out_page, "s_out_page", B * H)
+    if n_commit is not None:
+        _need(n_commit, "n_commit", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, n_tok, H, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, n_tok, H, d))
+    if workspace is None:
+        workspace = torch.empty(decode_paged_workspace_size(n_pages), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_decode_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool), n_pages,
+                                    _ptr(s_in_page), _ptr(s_out_page), _ptr(n_commit), _ptr(o), B, n_tok, H, d,
+                                    _ptr(workspace), ws_bytes, _ptr(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_decode_paged")
+    return o
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

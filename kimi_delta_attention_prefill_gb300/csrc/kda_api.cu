@@ -88,12 +88,23 @@ size_t kda_prefill_workspace_size(int n_seq, int H, int d, int64_t total_tokens,
 }  // extern "C"
 
 namespace {
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Host checks shared by the paged entry points.
+kda_status check_pool(const float* pool, int64_t n_pages) {
+  if (n_pages < 0 || n_pages > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (n_pages > 0 && !pool) return KDA_ERR_INVALID_ARG;
+  return aligned(pool, 16) ? KDA_OK : KDA_ERR_ALIGNMENT;
+}
+
+// `pages` is nullptr for contiguous states; otherwise S_in / S_out / ckpts are unused and
+// the page check runs in the workspace after the split path's part.
 kda_status prefill_impl(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g, const float* beta,
                         const kda_bf16* gate, const float* norm_weight, float eps, const float* S_in,
                         const int32_t* cu_seqlens, int n_seq, int64_t total_tokens, const int32_t* ckpt_off,
                         const int32_t* ckpt_pos, int64_t n_ckpt, kda_bf16* o, float* S_out, float* ckpts, int H,
                         int d, int n_segments, void* workspace, size_t workspace_bytes, int* dev_status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const kda::PageTables* pages = nullptr) {
   if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
   if (n_seq < 0 || H < 0 || total_tokens < 0 || n_ckpt < 0 || n_segments < 0) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0x7fffffffLL || static_cast<int64_t>(n_seq) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
@@ -102,16 +113,22 @@ kda_status prefill_impl(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
   if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
   if (ckpt_off == nullptr && n_ckpt != 0) return KDA_ERR_INVALID_ARG;
-  if (ckpt_off != nullptr && n_ckpt > 0 && (!ckpt_pos || !ckpts)) return KDA_ERR_INVALID_ARG;
+  if (ckpt_off != nullptr && n_ckpt > 0 && (!ckpt_pos || !(pages ? pages->ckpt != nullptr : ckpts != nullptr)))
+    return KDA_ERR_INVALID_ARG;
+  if (pages && (static_cast<int64_t>(n_seq) + n_ckpt) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(o, 16) ||
       !aligned(S_in, 16) || !aligned(S_out, 16) || !aligned(ckpts, 16) || !aligned(beta, 4) ||
       !aligned(cu_seqlens, 4) || !aligned(ckpt_off, 4) || !aligned(ckpt_pos, 4) || !aligned(dev_status, 4) ||
       !aligned(workspace, 256))
     return KDA_ERR_ALIGNMENT;
+  // the page check's part of the workspace does not depend on the device
+  if (pages && (workspace == nullptr || workspace_bytes < kda::page_check_bytes(pages->n_pages)))
+    return KDA_ERR_WORKSPACE;
   int sms = 0;
   kda_status st = current_device(&sms);
   if (st != KDA_OK) return st;
-  const size_t need = kda::prefill_workspace_bytes(n_seq, H, total_tokens, n_segments, sms);
+  const size_t split = kda::prefill_workspace_bytes(n_seq, H, total_tokens, n_segments, sms);
+  const size_t need = pages ? up256(split) + kda::page_check_bytes(pages->n_pages) : split;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
   kda::PrefillArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S_in = S_in;
@@ -121,6 +138,16 @@ kda_status prefill_impl(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
   a.o = o; a.S_out = S_out; a.ckpts = ckpts; a.H = H; a.n_segments = n_segments;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = dev_status; a.stream = stream;
   a.gate = gate; a.norm_weight = norm_weight; a.eps = eps;
+  if (pages) {
+    void* pws = static_cast<uint8_t*>(workspace) + up256(split);
+    a.pages = *pages;
+    a.pages.ckpt = a.ckpt_off ? pages->ckpt : nullptr;
+    a.pages.fail = static_cast<const int*>(pws);
+    a.S_in = nullptr; a.S_out = nullptr; a.ckpts = nullptr;
+    cudaError_t e = kda::launch_page_check(pages->in, pages->out, static_cast<int64_t>(n_seq) * H, a.pages.ckpt,
+                                           n_ckpt * H, pages->n_pages, pws, dev_status, stream);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+  }
   cudaError_t e = kda::launch_prefill(a, sms);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -150,6 +177,69 @@ kda_status kda_prefill_gated(const kda_bf16* q, const kda_bf16* k, const kda_bf1
   return prefill_impl(q, k, v, g, beta, gate, norm_weight, eps, S_in, cu_seqlens, n_seq, total_tokens, ckpt_off,
                       ckpt_pos, n_ckpt, y, S_out, ckpts, H, d, n_segments, workspace, workspace_bytes, dev_status,
                       stream);
+}
+
+size_t kda_prefill_paged_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int n_segments,
+                                        int64_t n_pages) {
+  if (d != KDA_HEAD_DIM || n_seq < 0 || H <= 0 || total_tokens < 0 || n_segments < 0 || n_pages < 0) return 0;
+  int sms = 0;
+  if (current_device(&sms) != KDA_OK) sms = 152;
+  return up256(kda::prefill_workspace_bytes(n_seq, H, total_tokens, n_segments, sms)) + kda::page_check_bytes(n_pages);
+}
+
+kda_status kda_prefill_paged(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                             const float* beta, const kda_bf16* gate, const float* norm_weight, float eps,
+                             float* state_pool, int64_t n_pages, const int32_t* s_in_page,
+                             const int32_t* s_out_page, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens,
+                             const int32_t* ckpt_off, const int32_t* ckpt_pos, int64_t n_ckpt,
+                             const int32_t* ckpt_page, kda_bf16* o, int H, int d, int n_segments, void* workspace,
+                             size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  kda_status st = check_pool(state_pool, n_pages);
+  if (st != KDA_OK) return st;
+  if (!aligned(s_in_page, 4) || !aligned(s_out_page, 4) || !aligned(ckpt_page, 4)) return KDA_ERR_ALIGNMENT;
+  if (gate) {
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(gate, 16) || !aligned(norm_weight, 16)) return KDA_ERR_ALIGNMENT;
+  }
+  kda::PageTables pt;
+  pt.pool = state_pool; pt.n_pages = n_pages; pt.in = s_in_page; pt.out = s_out_page; pt.ckpt = ckpt_page;
+  return prefill_impl(q, k, v, g, beta, gate, gate ? norm_weight : nullptr, gate ? eps : 0.f, nullptr, cu_seqlens,
+                      n_seq, total_tokens, ckpt_off, ckpt_pos, n_ckpt, o, nullptr, nullptr, H, d, n_segments,
+                      workspace, workspace_bytes, dev_status, stream, &pt);
+}
+
+size_t kda_decode_paged_workspace_size(int64_t n_pages) {
+  return n_pages < 0 ? 0 : kda::page_check_bytes(n_pages);
+}
+
+kda_status kda_decode_paged(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                            const float* beta, float* state_pool, int64_t n_pages, const int32_t* s_in_page,
+                            const int32_t* s_out_page, const int32_t* n_commit, float* o, int B, int n_tok, int H,
+                            int d, void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (n_tok < 1 || n_tok > KDA_MAX_DECODE_TOKENS) return KDA_ERR_UNSUPPORTED;
+  if (B < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  kda_status st = check_pool(state_pool, n_pages);
+  if (st != KDA_OK) return st;
+  if (B == 0 || H == 0) return KDA_OK;
+  if (!q || !k || !v || !g || !beta || !o || !s_in_page) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(o, 16) ||
+      !aligned(beta, 4) || !aligned(n_commit, 4) || !aligned(dev_status, 4) || !aligned(s_in_page, 4) ||
+      !aligned(s_out_page, 4) || !aligned(workspace, 256))
+    return KDA_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < kda::page_check_bytes(n_pages)) return KDA_ERR_WORKSPACE;
+  if ((st = current_device(nullptr)) != KDA_OK) return st;
+  const int64_t units = static_cast<int64_t>(B) * H;
+  // in place (no out table): every unit writes its own entry page
+  cudaError_t e = kda::launch_page_check(s_in_page, s_out_page ? s_out_page : s_in_page, units, nullptr, 0, n_pages,
+                                         workspace, dev_status, stream);
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  kda::PageTables pt;
+  pt.pool = state_pool; pt.n_pages = n_pages; pt.in = s_in_page; pt.out = s_out_page;
+  pt.fail = static_cast<const int*>(workspace);
+  e = kda::launch_decode(q, k, v, g, beta, nullptr, n_commit, o, B, n_tok, H, dev_status, stream, pt);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // extern "C"

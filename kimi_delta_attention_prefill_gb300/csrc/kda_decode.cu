@@ -14,6 +14,12 @@
 // per load, all 16 loads in flight at once, and the reductions over d_k are a
 // thread-local sum over 16 rows followed by three xor-shuffles across the 8 row
 // groups: no shared-memory reduction and no cross-warp synchronisation.
+//
+// Paged state (kda_decode_paged): the state is read from page in[u] of a pool of 64 KiB
+// pages (-1: a zero state) and the committed state written to page out[u] (in place when
+// there is no out table, no write for -1).  A destination other than the source always
+// receives the state after n_commit tokens, the entry state itself when n_commit = 0
+// (copy on write: a shared cached state is never modified).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -41,7 +47,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
               const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
               float* __restrict__ S, const int32_t* __restrict__ n_commit, float* __restrict__ o, int n_tok,
-              int H, int* __restrict__ status) {
+              int H, int* __restrict__ status, const PageTables pg) {
   __shared__ DecodeSmem sm;
   const int unit = blockIdx.x;  // b * H + h
   const int b = unit / H, h = unit - b * H;
@@ -49,21 +55,45 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
   const int warp = tid >> 5, lane = tid & 31;
   const int c4 = lane & 3, r0 = lane >> 2;
   const int col = warp * 16 + c4 * 4;
+  if (pg.fail && *pg.fail) return;  // the page check refused the call: nothing is written
+
+  // source and destination of this unit's state
+  const float4* Sin;
+  float4* Sout;
+  if (pg.pool) {
+    const int32_t pi = pg.in ? pg.in[unit] : -1;
+    const int32_t po = pg.out ? pg.out[unit] : pi;
+    if (pi < -1 || pi >= pg.n_pages || po < -1 || po >= pg.n_pages) {
+      if (tid == 0) report_status(status, 7 /* KDA_ERR_DEVICE_CHECK */);
+      return;
+    }
+    Sin = pi >= 0 ? reinterpret_cast<const float4*>(pg.pool + pi * kStateFloats) : nullptr;
+    Sout = po >= 0 ? reinterpret_cast<float4*>(pg.pool + po * kStateFloats) : nullptr;
+  } else {
+    Sout = reinterpret_cast<float4*>(S + static_cast<int64_t>(unit) * kD * kD);
+    Sin = Sout;
+  }
 
   int nc = n_tok;
+  bool commit_ok = true;
   if (n_commit) {
     nc = n_commit[b];
     if (nc < 0 || nc > n_tok) {
       if (tid == 0) report_status(status, 7 /* KDA_ERR_DEVICE_CHECK */);
       nc = 0;  // leave this sequence's state untouched; outputs are still produced
+      commit_ok = false;
     }
   }
 
   // Issue the state loads first: 16 independent 16-byte loads per thread.
-  float4* Sh = reinterpret_cast<float4*>(S + static_cast<int64_t>(unit) * kD * kD);
   float4 s[kRowsPerThread];
 #pragma unroll
-  for (int m = 0; m < kRowsPerThread; ++m) s[m] = Sh[((r0 + 8 * m) * kD + col) >> 2];
+  for (int m = 0; m < kRowsPerThread; ++m)
+    s[m] = Sin ? Sin[((r0 + 8 * m) * kD + col) >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (nc == 0 && commit_ok && Sout && Sout != Sin) {  // no token committed: the destination takes the entry state
+#pragma unroll
+    for (int m = 0; m < kRowsPerThread; ++m) __stcs(&Sout[((r0 + 8 * m) * kD + col) >> 2], s[m]);
+  }
 
   // Stage this head's inputs for all tokens (tiny) while the state streams in.
   for (int e = tid; e < n_tok * kD; e += kThreads) {
@@ -118,9 +148,9 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
       const float kk = sm.k[i][r0 + 8 * m];
       s[m].x += kk * u.x; s[m].y += kk * u.y; s[m].z += kk * u.z; s[m].w += kk * u.w;
     }
-    if (i + 1 == nc) {
+    if (i + 1 == nc && Sout) {
 #pragma unroll
-      for (int m = 0; m < kRowsPerThread; ++m) __stcs(&Sh[((r0 + 8 * m) * kD + col) >> 2], s[m]);
+      for (int m = 0; m < kRowsPerThread; ++m) __stcs(&Sout[((r0 + 8 * m) * kD + col) >> 2], s[m]);
     }
   }
 }
@@ -129,12 +159,12 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, float* S,
                           const int32_t* n_commit, float* o, int B, int n_tok, int H, int* status,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const PageTables& pages) {
   const int64_t units = static_cast<int64_t>(B) * H;
   if (units == 0) return cudaSuccess;
   decode_kernel<<<static_cast<unsigned>(units), kThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), g, beta, S, n_commit, o, n_tok, H, status);
+      static_cast<const __nv_bfloat16*>(v), g, beta, S, n_commit, o, n_tok, H, status, pages);
   return cudaGetLastError();
 }
 

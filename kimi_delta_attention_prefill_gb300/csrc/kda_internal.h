@@ -16,9 +16,32 @@ __device__ __forceinline__ void report_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+constexpr int64_t kStateFloats = static_cast<int64_t>(kHeadDim) * kHeadDim;  // one page / one head's state
+
+// Paged state: a pool of pages, each one head's 128 x 128 fp32 state (64 KiB, row = d_k),
+// addressed through int32 page tables; -1 = no page (a zero entry state, or no write).
+struct PageTables {
+  float* pool = nullptr;  // nullptr: contiguous addressing
+  int64_t n_pages = 0;
+  const int32_t* in = nullptr;    // [units] entry / read page
+  const int32_t* out = nullptr;   // [units] final / written page
+  const int32_t* ckpt = nullptr;  // [n_ckpt * H] checkpoint pages (prefill)
+  const int* fail = nullptr;      // set by the page check: the kernels then do nothing
+};
+
+// Workspace of the page check: a failure word, then an owner table of n_pages int32.
+__host__ inline size_t page_check_bytes(int64_t n_pages) { return 256 + 4 * static_cast<size_t>(n_pages); }
+
+// Claims every written page for its writer (a page may be written once per call) and
+// then checks every read page: it may be written only by its own unit (in place).
+// Writers: out[u] is writer u, ckpt[j] writer n_units + j.  On a violation or a page
+// outside [-1, n_pages) it sets the failure word and reports KDA_ERR_DEVICE_CHECK.
+cudaError_t launch_page_check(const int32_t* in, const int32_t* out, int64_t n_units, const int32_t* ckpt,
+                              int64_t n_ckpt_entries, int64_t n_pages, void* ws, int* status, cudaStream_t stream);
+
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, float* S,
                           const int32_t* n_commit, float* o, int B, int n_tok, int H, int* status,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const PageTables& pages = PageTables());
 
 struct PrefillArgs {
   const void* q;
@@ -40,6 +63,7 @@ struct PrefillArgs {
   float eps = 0.f;
   float* S_out;
   float* ckpts;
+  PageTables pages;  // paged S_in / S_out / checkpoints when pages.pool is set
   int H;
   int n_segments;  // 0 = planner, k >= 1 forced
   void* workspace;

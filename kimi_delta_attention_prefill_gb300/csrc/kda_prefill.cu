@@ -134,6 +134,7 @@ struct KParams {
   float eps;
   float* S_out;
   float* ckpts;
+  PageTables pg;  // paged S_in / S_out / checkpoints when pg.pool is set
   int* status;
   int n_seq, H;
   int64_t total_tokens;
@@ -181,6 +182,25 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
     }
   }
   return true;
+}
+
+// Paged mode: every page a work item may touch lies in [-1, n_pages).
+__device__ bool pages_ok(const KParams& p, int seq, int h, int cb, int ce) {
+  const int64_t unit = static_cast<int64_t>(seq) * p.H + h;
+  auto ok = [&](int32_t pg) { return pg >= -1 && pg < p.pg.n_pages; };
+  if (p.pg.in && !ok(p.pg.in[unit])) return false;
+  if (p.pg.out && !ok(p.pg.out[unit])) return false;
+  if (p.pg.ckpt)
+    for (int j = cb; j < ce; ++j)
+      if (!ok(p.pg.ckpt[static_cast<int64_t>(j) * p.H + h])) return false;
+  return true;
+}
+
+// Page `idx` of a table as a state pointer (nullptr for -1 or no table).
+__device__ __forceinline__ float* page_ptr(const KParams& p, const int32_t* table, int64_t idx) {
+  if (!table) return nullptr;
+  const int32_t pg = table[idx];
+  return pg >= 0 ? p.pg.pool + static_cast<int64_t>(pg) * kStateFloats : nullptr;
 }
 
 // ------------------------------------------------------------- INV = (I + L)^-1
@@ -963,7 +983,8 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       const int pos = min((cidx + 1) * kChunk, w.len);
       float* ckdst = nullptr;
       if (ck < w.ck_end && p.ckpt_pos[ck] == pos) {
-        ckdst = p.ckpts + (static_cast<int64_t>(ck) * p.H + w.h) * (kHeadDim * kHeadDim);
+        const int64_t e = static_cast<int64_t>(ck) * p.H + w.h;
+        ckdst = p.pg.pool ? page_ptr(p, p.pg.ckpt, e) : p.ckpts + e * (kHeadDim * kHeadDim);
         ++ck;
       }
       float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
@@ -1021,9 +1042,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   Work w;
   w.seq = it.x;
   w.h = blockIdx.y;
+  if (p.pg.fail && *p.pg.fail) return;  // the page check refused the call: nothing is written
   if (tid == 0) {
     int64_t bos; int len, cb, ce;
-    const bool ok = check_sequence(p, w.seq, bos, len, cb, ce);
+    bool ok = check_sequence(p, w.seq, bos, len, cb, ce);
+    if (ok && p.pg.pool) ok = pages_ok(p, w.seq, w.h, cb, ce);
     ctrl[CTRL_VALID] = ok ? 1 : 0;
     if (!ok) report_status(p.status, 7 /* KDA_ERR_DEVICE_CHECK */);
   }
@@ -1040,8 +1063,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int nch = (w.len + kChunk - 1) / kChunk;
     w.c0 = it.y;
     w.c1 = it.z < 0 ? nch : it.z;
-    float* s_out = p.S_out ? p.S_out + unit * (kHeadDim * kHeadDim) : nullptr;
-    const float* s_in = p.S_in ? p.S_in + unit * (kHeadDim * kHeadDim) : nullptr;
+    float* s_out;
+    const float* s_in;
+    if (p.pg.pool) {
+      s_out = page_ptr(p, p.pg.out, unit);
+      s_in = page_ptr(p, p.pg.in, unit);
+    } else {
+      s_out = p.S_out ? p.S_out + unit * (kHeadDim * kHeadDim) : nullptr;
+      s_in = p.S_in ? p.S_in + unit * (kHeadDim * kHeadDim) : nullptr;
+    }
     switch (mode) {
       case kModeFirst: w.entry = s_in; w.s_out = slot_buf(0); break;
       case kModeZero: w.entry = nullptr; w.s_out = slot_buf(0); break;
@@ -1145,6 +1175,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.beta = a.beta; p.S_in = a.S_in; p.cu = a.cu_seqlens; p.ckpt_off = a.ckpt_off; p.ckpt_pos = a.ckpt_pos;
   p.o = static_cast<__nv_bfloat16*>(a.o); p.S_out = a.S_out; p.ckpts = a.ckpts; p.status = a.status;
   p.gate = static_cast<const __nv_bfloat16*>(a.gate); p.norm_weight = a.norm_weight; p.eps = a.eps;
+  p.pg = a.pages;
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
   static bool attr_set = false;
   if (!attr_set) {

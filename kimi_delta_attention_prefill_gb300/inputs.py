@@ -144,6 +144,20 @@ def make_output_stage(T, H, d=128, seed=0, device="cpu"):
     return gate, weight
 
 
+def make_page_tables(counts, n_pages, seed=0):
+    """Distinct pages for several int32 page tables: ``counts`` entries each, drawn without
+    replacement from a seeded permutation of ``range(n_pages)`` (scattered over the pool)."""
+    total = sum(int(c) for c in counts)
+    if total > n_pages:
+        raise ValueError(f"{total} pages asked of a pool of {n_pages}")
+    perm = torch.randperm(n_pages, generator=_gen("cpu", 104729 + seed)).to(torch.int32)
+    out, at = [], 0
+    for c in counts:
+        out.append(perm[at:at + int(c)].clone())
+        at += int(c)
+    return out
+
+
 def varlen_lengths(n_seq, lo, hi, seed):
     """Sequence lengths uniform on {lo, ..., hi}, drawn first from ``seed``."""
     gen = _gen("cpu", seed)

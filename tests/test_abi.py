@@ -147,3 +147,60 @@ def test_workspace_sizes(lib):
     assert kda.prefill_workspace_size(4, 2, 10000, n_segments=1) == 0
     assert kda.prefill_workspace_size(4, 2, 10000, n_segments=3) > 0
     assert kda.prefill_workspace_size(4, 2, 10000, n_segments=-1) == 0
+
+
+def _prefill_paged(lib, pool=0x20000, n_pages=16, s_in=0xB000, s_out=0xB100, ckpt_off=None, ckpt_pos=None,
+                   n_ckpt=0, ckpt_page=None, ws=0x40000, ws_bytes=1 << 20, gate=None, eps=1e-5, n_seq=1, H=2):
+    return lib.kda_prefill_paged(P(0x1000), P(0x1100), P(0x1200), P(0x1300), P(0x1400), P(gate) if gate else None,
+                                 None, eps, P(pool) if pool else None, n_pages, P(s_in) if s_in else None,
+                                 P(s_out) if s_out else None, P(0x9000), n_seq, 64, ckpt_off, ckpt_pos, n_ckpt,
+                                 P(ckpt_page) if ckpt_page else None, P(0x1500), H, 128, 0,
+                                 P(ws) if ws else None, ws_bytes, None, None)
+
+
+def test_prefill_paged_host_validation(lib):
+    """Paged states ("部署 Kimi K3 ..." 3): a pool, int32 page tables, a workspace that always
+    holds the page check; bad pools, tables and workspaces are rejected on the host."""
+    assert _prefill_paged(lib, n_pages=-1) == INVALID
+    assert _prefill_paged(lib, n_pages=1 << 31) == INVALID
+    assert _prefill_paged(lib, pool=0) == INVALID
+    assert _prefill_paged(lib, pool=0x20008) == ALIGNMENT
+    assert _prefill_paged(lib, s_in=0xB002) == ALIGNMENT
+    assert _prefill_paged(lib, ws=0x40010) == ALIGNMENT
+    assert _prefill_paged(lib, ws=0, ws_bytes=0) == WORKSPACE
+    assert _prefill_paged(lib, ws_bytes=100) == WORKSPACE
+    assert _prefill_paged(lib, ckpt_off=P(0xA000), ckpt_pos=P(0xA100), n_ckpt=2) == INVALID  # no checkpoint pages
+    assert _prefill_paged(lib, gate=0x1700, eps=-1.0) == INVALID
+    assert _prefill_paged(lib, gate=0x1702) == ALIGNMENT
+    assert _prefill_paged(lib, n_seq=0) == OK
+    if not HAS_GPU:
+        assert _prefill_paged(lib) in (CUDA, UNSUPPORTED)
+        assert _prefill_paged(lib, s_in=0, s_out=0) in (CUDA, UNSUPPORTED)
+
+
+def _decode_paged(lib, pool=0x20000, n_pages=16, s_in=0xB000, s_out=None, ws=0x40000, ws_bytes=1 << 20, n_tok=1,
+                  B=2, H=2):
+    return lib.kda_decode_paged(P(0x1000), P(0x1100), P(0x1200), P(0x1300), P(0x1400), P(pool) if pool else None,
+                                n_pages, P(s_in) if s_in else None, P(s_out) if s_out else None, None, P(0x1500),
+                                B, n_tok, H, 128, P(ws) if ws else None, ws_bytes, None, None)
+
+
+def test_decode_paged_host_validation(lib):
+    assert _decode_paged(lib, n_tok=5) == UNSUPPORTED
+    assert _decode_paged(lib, n_pages=-3) == INVALID
+    assert _decode_paged(lib, pool=0) == INVALID
+    assert _decode_paged(lib, s_in=0) == INVALID
+    assert _decode_paged(lib, s_out=0xB102) == ALIGNMENT
+    assert _decode_paged(lib, ws=0) == WORKSPACE
+    assert _decode_paged(lib, ws_bytes=256) == WORKSPACE  # 16 pages need 256 + 64 bytes
+    assert _decode_paged(lib, B=0) == OK
+    if not HAS_GPU:
+        assert _decode_paged(lib) in (CUDA, UNSUPPORTED)
+
+
+def test_paged_workspace_sizes(lib):
+    assert kda.decode_paged_workspace_size(0) == 256
+    assert kda.decode_paged_workspace_size(1000) == 256 + 4000
+    assert kda.prefill_paged_workspace_size(1, 96, 8192, n_pages=10) == 256 + 40  # no split at 96 heads
+    split = kda.prefill_workspace_size(4, 2, 10000, n_segments=3)
+    assert kda.prefill_paged_workspace_size(4, 2, 10000, n_pages=7, n_segments=3) == (split + 255) // 256 * 256 + 284
