@@ -286,8 +286,54 @@ def run_ours(args, world, rank, local):
     dms = d0.elapsed_time(d1) / dsteps
     n_units = 256 * H
     dec_bytes = n_units * (DECODE_STATE_BYTES + DECODE_IO_BYTES)
-    dec_gbs = n_units * DECODE_STATE_BYTES / (dms / 1e-3) / 1e9 if False else n_units * DECODE_STATE_BYTES / (dms / 1e3) / 1e9
+    dec_gbs = n_units * DECODE_STATE_BYTES / (dms / 1e3) / 1e9
     dec_all_gbs = dec_bytes / (dms / 1e3) / 1e9
+
+    # paged states: the decode step reading its 256 x 96 states from scattered pages of a
+    # pool and writing the committed states to other scattered pages (speculation from
+    # shared snapshots), page check included; and the 8192 x 96 prefill with its entry and
+    # final states in pages.  Same algorithmic bytes as the contiguous calls.
+    n_pool = 2 * n_units + 1024
+    pin, pout, pin_pf, pout_pf = inputs.make_page_tables([n_units, n_units, H, H], n_pool, seed=5)
+    pool = torch.zeros((n_pool, D, D), dtype=torch.float32, device=dev)
+    pool[pin.long().to(dev)] = dx.S0.reshape(-1, D, D)
+    pin, pout, pin_pf, pout_pf = (t.to(dev) for t in (pin, pout, pin_pf, pout_pf))
+    pws = torch.empty(kda.decode_paged_workspace_size(n_pool), dtype=torch.uint8, device=dev)
+    pfws = torch.empty(kda.prefill_paged_workspace_size(1, H, T, n_pool), dtype=torch.uint8, device=dev)
+
+    def pdstep():
+        kda.decode_paged(dx.q, dx.k, dx.v, dx.g, dx.beta, pool, pin, pout, o=od, workspace=pws, stream=stream)
+
+    def ppstep():
+        kda.prefill_paged(x.q, x.k, x.v, x.g, x.beta, cu, pool, s_in_page=pin_pf, s_out_page=pout_pf, o=o,
+                          workspace=pfws, stream=stream)
+
+    def timed(fn, n):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    pdms = timed(pdstep, dsteps)
+    ppms = timed(ppstep, args.steps)
+    pd_gbs = n_units * DECODE_STATE_BYTES / (pdms / 1e3) / 1e9
+    paged = {"metric": "KDA paged decode state GB/s (256 x 96 heads, 1 token, scattered pages in a "
+                       f"{n_pool}-page pool, committed states to other pages, page check included)",
+             "value": pd_gbs, "unit": "GB/s", "us_per_step": pdms * 1e3, "vs_contiguous": dms / pdms,
+             "roofline": {"bound": "hbm", "achieved": dec_bytes / (pdms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": dec_bytes / (pdms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                          "traffic": None, "kernel": "decode_kernel (paged) + page check",
+                          "bytes_per_launch": dec_bytes},
+             "prefill": {"metric": "KDA paged prefill tokens/s (8192 x 96, entry and final states in pages)",
+                         "value": T / (ppms / 1e3), "unit": "tokens/s", "ms_per_step": ppms,
+                         "vs_contiguous": ms_local / ppms}}
+    del pool
 
     # end to end through the public call, host buffers: pinned H2D of the step's inputs,
     # the prefill, D2H of o and the final state
@@ -353,6 +399,7 @@ def run_ours(args, world, rank, local):
                                     "traffic": None if DECODE_TRAFFIC_PER_HEAD is None else DECODE_TRAFFIC_PER_HEAD * H,
                                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes}},
             "gated": gated,
+            "paged": paged,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_prefill * args.steps,
             "clocks": clk.summary(),
