@@ -339,3 +339,154 @@ def pin_epilogue_eps_closed_form():
 
 
 ALL_PINS += [pin_epilogue_hand_values, pin_epilogue_invariants, pin_epilogue_eps_closed_form]
+
+
+# --------------------------------------------------------------------- decode front end
+# oracle/frontend.py: "Kimi K3 的架構 ... 服務性能" section 7 (short causal convolution, q/k L2
+# normalisation, alpha and beta gates) and "Kimi K3.1 Pro 架构完全拆解" 3.2 (bounded decay
+# gate) and 3.4 (fused replay step).
+
+def pin_frontend_conv_against_numpy():
+    """Each channel of the causal convolution equals numpy.convolve of (cache, x) with the
+    channel's filter, taken at the positions of the n tokens; W = 1 with tap 1 is the
+    identity; an input never changes an earlier output."""
+    from oracle.frontend import short_conv
+    rng = np.random.default_rng(11)
+    for W in (1, 2, 3, 4):
+        x = rng.standard_normal((6, 5))
+        cache = rng.standard_normal((W - 1, 5))
+        w = rng.standard_normal((5, W))
+        y = short_conv(x, cache, w)
+        full = np.concatenate([cache, x], 0)
+        for c in range(5):
+            want = np.convolve(full[:, c], w[c])[W - 1:W - 1 + 6]
+            assert np.allclose(y[:, c], want, rtol=1e-13, atol=1e-13), (W, c)
+        x2 = x.copy()
+        x2[3] += 10.0
+        assert np.array_equal(short_conv(x2, cache, w)[:3], y[:3])
+    x = rng.standard_normal((4, 3))
+    assert np.array_equal(short_conv(x, np.zeros((0, 3)), np.ones((3, 1))), x)
+
+
+def pin_frontend_silu_and_l2():
+    """SiLU: silu(0) = 0, silu(1) = 1 / (1 + e^-1), silu(x) -> x for large x and -> 0 for very
+    negative x.  L2: (3, 4) -> (0.6, 0.8), unit norm, scale invariance, zero stays zero."""
+    from oracle.frontend import l2_normalize, short_conv, silu
+    assert silu(0.0) == 0.0
+    assert np.isclose(silu(1.0), 1.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+    assert np.isclose(silu(40.0), 40.0, rtol=1e-15) and abs(silu(-40.0)) < 1e-15
+    x = np.array([[0.5, -1.0]])
+    y = short_conv(x, np.zeros((0, 2)), np.ones((2, 1)), act="silu")
+    assert np.allclose(y, [[0.5 / (1 + np.exp(-0.5)), -1.0 / (1 + np.exp(1.0))]], rtol=1e-15)
+    assert np.allclose(l2_normalize(np.array([3.0, 4.0])), [0.6, 0.8], rtol=1e-15)
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal((4, 128))
+    u = l2_normalize(v)
+    assert np.allclose(np.linalg.norm(u, axis=-1), 1.0, rtol=1e-14)
+    assert np.allclose(l2_normalize(3.7 * v), u, rtol=1e-14)
+    assert np.array_equal(l2_normalize(np.zeros((2, 8))), np.zeros((2, 8)))
+
+
+def pin_frontend_gates():
+    """g = g_min Sigmoid(e^A z): z = 0 gives g_min / 2; z = ln 3, A = 0 gives Sigmoid = 3/4,
+    g = -3.75 at g_min = -5; A rescales z (g(z, A) = g(z e^A, 0)); g stays in (g_min, 0) and
+    alpha = e^g >= e^g_min.  beta = Sigmoid(b): 1/2 at 0, 3/4 at ln 3, b -> -b gives 1 - beta."""
+    from oracle.frontend import beta_gate, decay_log
+    assert decay_log(0.0, 0.3) == -2.5
+    assert np.isclose(decay_log(np.log(3.0), 0.0), -3.75, rtol=1e-15)
+    assert np.isclose(decay_log(np.log(3.0), 0.0, g_min=-2.0), -1.5, rtol=1e-15)
+    rng = np.random.default_rng(13)
+    z = rng.standard_normal(1000) * 3
+    a = rng.standard_normal(1000)
+    assert np.allclose(decay_log(z, a), decay_log(z * np.exp(a), 0.0), rtol=1e-14)
+    g = decay_log(z, a)
+    assert np.all(g <= 0) and np.all(g >= -5.0) and np.all(np.exp(g) >= np.exp(-5.0))
+    mid = np.abs(z * np.exp(a)) < 30  # away from the sigmoid's fp64 saturation the bounds are strict
+    assert np.all(g[mid] < 0) and np.all(g[mid] > -5.0)
+    assert beta_gate(0.0) == 0.5 and np.isclose(beta_gate(np.log(3.0)), 0.75, rtol=1e-15)
+    assert np.allclose(beta_gate(-z), 1.0 - beta_gate(z), rtol=1e-13, atol=1e-15)
+
+
+def _frontend_case(rng, B=2, n=4, H=2, d=16, W=4):
+    qp, kp, vp = (rng.standard_normal((B, n, H, d)) for _ in range(3))
+    conv_w = rng.standard_normal((3, H, d, W)) * 0.5
+    cache = rng.standard_normal((B, H, 3, W - 1, d))
+    z = rng.standard_normal((B, n, H, d)) - 2.0
+    a_log = rng.standard_normal(H) * 0.3
+    b = rng.standard_normal((B, n, H))
+    S = rng.standard_normal((B, H, d, d)) * 0.1
+    return qp, kp, vp, conv_w, cache, z, a_log, b, S
+
+
+def pin_frontend_replay_identities():
+    """A step over tokens 0..1 followed by a step over tokens 2..4 (from the state and cache
+    the first left) gives the outputs and final state of one step over tokens 0..4; a step
+    that commits only its first m tokens leaves the state and cache of a step over those m
+    tokens alone; n_commit = 0 leaves both unchanged."""
+    from oracle.frontend import decode_step
+    rng = np.random.default_rng(14)
+    qp, kp, vp, conv_w, cache, z, a_log, b, S = _frontend_case(rng, n=5)
+    for act in ("none", "silu"):
+        one = decode_step(qp, kp, vp, conv_w, cache, z, a_log, b, S, act=act)
+        sl = lambda t, a, e: t[:, a:e]
+        r1 = decode_step(sl(qp, 0, 2), sl(kp, 0, 2), sl(vp, 0, 2), conv_w, cache, sl(z, 0, 2), a_log, sl(b, 0, 2), S,
+                         act=act)
+        r2 = decode_step(sl(qp, 2, 5), sl(kp, 2, 5), sl(vp, 2, 5), conv_w, r1["conv_cache"], sl(z, 2, 5), a_log,
+                         sl(b, 2, 5), r1["S"], act=act)
+        assert np.allclose(np.concatenate([r1["o"], r2["o"]], 1), one["o"], rtol=1e-11, atol=1e-12)
+        assert np.allclose(r2["S"], one["S"], rtol=1e-11, atol=1e-12)
+        assert np.allclose(r2["conv_cache"], one["conv_cache"], rtol=0, atol=0)
+    part = decode_step(qp[:, :4], kp[:, :4], vp[:, :4], conv_w, cache, z[:, :4], a_log, b[:, :4], S,
+                       n_commit=np.array([2, 0]))
+    two = decode_step(qp[:, :2], kp[:, :2], vp[:, :2], conv_w, cache, z[:, :2], a_log, b[:, :2], S)
+    assert np.allclose(part["S"][0], two["S"][0], rtol=1e-13, atol=1e-15)
+    assert np.array_equal(part["conv_cache"][0], two["conv_cache"][0])
+    assert np.array_equal(part["S"][1], S[1]) and np.array_equal(part["conv_cache"][1], cache[1])
+    assert np.allclose(part["o"][:, :2], two["o"], rtol=1e-13, atol=1e-15)  # outputs never depend on n_commit
+
+
+def pin_frontend_recurrence_against_c_oracle():
+    """The batched numpy recurrence equals the C oracle's decode (an independent
+    implementation of the same definition) on the same fp32-representable inputs."""
+    import oracle
+    from oracle.frontend import l2_normalize, recurrence
+    rng = np.random.default_rng(15)
+    B, n, H, d = 3, 4, 2, 128
+    f32 = lambda t: np.asarray(t, np.float32)
+    q = f32(l2_normalize(rng.standard_normal((B, n, H, d))))
+    k = f32(l2_normalize(rng.standard_normal((B, n, H, d))))
+    v = f32(rng.standard_normal((B, n, H, d)))
+    g = f32(-5.0 / (1.0 + np.exp(-(rng.standard_normal((B, n, H, d)) - 2.0))))
+    beta = f32(1.0 / (1.0 + np.exp(-rng.standard_normal((B, n, H)))))
+    S = f32(rng.standard_normal((B, H, d, d)) * 0.05)
+    nc = np.array([4, 1, 0], np.int32)
+    o, Sn = recurrence(q, k, v, g, beta, S, nc)
+    ref = oracle.decode(q, k, v, g, beta, S, nc)
+    assert np.allclose(o, ref["o"], rtol=1e-10, atol=1e-12)
+    assert np.allclose(Sn, ref["S"], rtol=1e-10, atol=1e-12)
+
+
+def pin_frontend_step_retrieval():
+    """The fused step's key reaches the recurrence unit-normalised: with beta = 1 (b large)
+    the delta rule makes the new state return the token's value, S_new^T k = v, exactly when
+    ||k|| = 1 ("Kimi K3 ... 服務性能" 4 and 7); the value is the convolution's output (identity
+    filter of width 1: v = vp) and the query and key have unit norm."""
+    from oracle.frontend import decode_step
+    rng = np.random.default_rng(16)
+    B, H, d = 2, 2, 32
+    qp, kp, vp = (rng.standard_normal((B, 1, H, d)) * 3 for _ in range(3))
+    ones = np.ones((3, H, d, 1))
+    z = rng.standard_normal((B, 1, H, d))
+    b = np.full((B, 1, H), 60.0)
+    S = rng.standard_normal((B, H, d, d))
+    r = decode_step(qp, kp, vp, ones, np.zeros((B, H, 3, 0, d)), z, np.zeros(H), b, S)
+    assert np.allclose(np.linalg.norm(r["k"], axis=-1), 1.0, rtol=1e-14)
+    assert np.allclose(np.linalg.norm(r["q"], axis=-1), 1.0, rtol=1e-14)
+    assert np.array_equal(r["v"], vp)
+    k, v = r["k"][:, 0], r["v"][:, 0]
+    assert np.allclose(np.einsum("bhij,bhi->bhj", r["S"], k), v, rtol=1e-12, atol=1e-12)
+
+
+ALL_PINS += [pin_frontend_conv_against_numpy, pin_frontend_silu_and_l2, pin_frontend_gates,
+             pin_frontend_replay_identities, pin_frontend_recurrence_against_c_oracle,
+             pin_frontend_step_retrieval]

@@ -84,3 +84,41 @@ def test_epilogue_mutant_is_caught(name, monkeypatch):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"mutant {name} passed every pin"
+
+
+FRONTEND_MUTANTS = {
+    "taps_reversed": ("y[..., i, :] += w[:, j] * full[..., W - 1 + i - j, :]",
+                      "y[..., i, :] += w[:, W - 1 - j] * full[..., W - 1 + i - j, :]"),
+    "conv_reads_ahead": ("full[..., W - 1 + i - j, :]", "full[..., min(W - 1 + i + j, full.shape[-2] - 1), :]"),
+    "silu_is_sigmoid": ("return x * sigmoid(x)", "return sigmoid(x)"),
+    "l2_without_sqrt": ("n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))", "n = np.sum(x * x, axis=-1, keepdims=True)"),
+    "gate_without_exp_scale": ("sigmoid(np.exp(np.asarray(a_log, np.float64)) * np.asarray(z, np.float64))",
+                               "sigmoid(np.asarray(a_log, np.float64) * np.asarray(z, np.float64))"),
+    "beta_raw": ("def beta_gate(b):\n    return sigmoid(b)", "def beta_gate(b):\n    return np.asarray(b, np.float64)"),
+    "cache_keeps_oldest": ("return full[..., full.shape[-2] - keep:, :]", "return full[..., :keep, :]"),
+    "decay_dropped": ("S = np.exp(g[:, i])[..., :, None] * S", "S = S"),
+    "k_not_normalised": ("k = l2_normalize(streams[1])", "k = streams[1]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FRONTEND_MUTANTS))
+def test_frontend_mutant_is_caught(name, monkeypatch):
+    import sys
+    import types
+    import oracle.frontend as real
+    old, new = FRONTEND_MUTANTS[name]
+    src = open(real.__file__).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mod = types.ModuleType("oracle.frontend")
+    mod.__package__ = "oracle"
+    exec(compile(src.replace(old, new), real.__file__, "exec"), mod.__dict__)
+    monkeypatch.setitem(sys.modules, "oracle.frontend", mod)
+    caught = []
+    for pin in (oracle_pins.pin_frontend_conv_against_numpy, oracle_pins.pin_frontend_silu_and_l2,
+                oracle_pins.pin_frontend_gates, oracle_pins.pin_frontend_replay_identities,
+                oracle_pins.pin_frontend_recurrence_against_c_oracle, oracle_pins.pin_frontend_step_retrieval):
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
