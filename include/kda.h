@@ -219,6 +219,44 @@ kda_status kda_decode_paged(const kda_bf16* q, const kda_bf16* k, const kda_bf16
                             int d, void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream);
 
 /*
+ * kda_decode_fused -- a decode / verify step from the layer's projected inputs, with its
+ * front end (and optionally its output stage) in the same kernel.
+ *
+ * "Kimi K3.1 Pro 架构完全拆解" section 3.4: for speculative decoding only the projected
+ * inputs are cached, and one fused kernel replays the accepted tokens (short convolution,
+ * input normalisation, gating, the recurrence, output normalisation) and writes the state
+ * back.  The steps ("Kimi K3 ... 服務性能" section 7; K3.1 page section 3.2), per (sequence b,
+ * token i, head h), channel c:
+ *     x~_i = sum_{j < W} conv_w[s, h, c, j] x_{i-j}     (x = qp, kp, vp for s = 0, 1, 2; inputs
+ *                                                        before token 0 come from conv_cache)
+ *     optionally x~ <- x~ Sigmoid(x~) (SiLU, conv_act = 1)
+ *     q = q~ / ||q~||,  k = k~ / ||k~||  (over the head's d channels; a zero vector stays 0)
+ *     alpha = exp(g_min Sigmoid(exp(a_log[h]) z)),  beta = Sigmoid(b)
+ *     then the recurrence, outputs and commit of kda_decode, and, with gate != NULL, the
+ *     output stage y = Sigmoid(gate) norm_weight o / sqrt(mean(o^2) + eps) in place of o.
+ * The pages print neither the convolution width, an activation after it, nor beta's
+ * activation: those are the readings above (W and the activation are arguments).
+ *
+ *   qp, kp, vp   [B, n_tok, H, d] bf16 projected inputs
+ *   conv_w       [3, H, d, W] fp32 filters (q, k, v), 1 <= W <= 4
+ *   conv_cache   [B, H, 3, W - 1, d] fp32: the W - 1 projected inputs before this step,
+ *                oldest first; on return those before token n_commit[b] (unchanged when
+ *                n_commit[b] = 0).  May be NULL when W = 1.
+ *   conv_act     0: none, 1: SiLU
+ *   z            [B, n_tok, H, d] fp32 decay-gate pre-activations;  a_log [H] fp32
+ *   g_min        the decay's lower bound, finite and < 0 (-5 on the pages)
+ *   b            [B, n_tok, H] fp32 beta logits
+ *   gate         [B, n_tok, H, d] bf16 output-gate logits, or NULL (o as kda_decode)
+ *   norm_weight  [d] fp32 or NULL (ones);  eps >= 0 and finite
+ *   S_state, n_commit, o, B, n_tok, H, d, dev_status, stream: as kda_decode
+ */
+kda_status kda_decode_fused(const kda_bf16* qp, const kda_bf16* kp, const kda_bf16* vp, const float* conv_w,
+                            float* conv_cache, int conv_width, int conv_act, const float* z, const float* a_log,
+                            float g_min, const float* b, const kda_bf16* gate, const float* norm_weight, float eps,
+                            float* S_state, const int32_t* n_commit, float* o, int B, int n_tok, int H, int d,
+                            int* dev_status, cudaStream_t stream);
+
+/*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
  *
  * This entry point has no counterpart on the pages; it exists for the library's users.

@@ -79,6 +79,9 @@ def library():
             lib.kda_decode_paged.restype = _c_int
             lib.kda_decode_paged.argtypes = ([_vp] * 6 + [_c_i64] + [_vp] * 4 + [_c_int] * 4 +
                                              [_vp, _c_sz, _vp, _vp])
+            lib.kda_decode_fused.restype = _c_int
+            lib.kda_decode_fused.argtypes = ([_vp] * 5 + [_c_int, _c_int] + [_vp, _vp, ctypes.c_float] + [_vp] * 3 +
+                                             [ctypes.c_float] + [_vp] * 3 + [_c_int] * 4 + [_vp, _vp])
             lib.kda_prefill_noalloc.restype = _c_int
             lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                                 [_c_int, _c_int, _c_int, _vp, _vp])
@@ -142,6 +145,49 @@ def decode(q, k, v, g, beta, S_state, n_commit=None, o=None, dev_status=None, st
                               _ptr(o), B, n_tok, H, d, _ptr(dev_status), _stream_handle(stream))
     if st != 0:
         raise KdaError(st, "kda_decode")
+    return o
+
+
+def decode_fused(qp, kp, vp, conv_w, conv_cache, z, a_log, b, S_state, n_commit=None, conv_act="none",
+                 g_min=-5.0, gate=None, norm_weight=None, eps=1e-5, o=None, dev_status=None, stream=None):
+    """A decode / verify step from projected inputs (``kda_decode_fused``): short causal
+    convolution (``conv_w`` ``[3, H, 128, W]``, ``conv_cache`` ``[B, H, 3, W-1, 128]``, updated
+    in place to the committed tokens), q / k L2 normalisation, alpha = exp(g_min
+    sigmoid(e^a_log z)), beta = sigmoid(b), the recurrence on ``S_state`` (in place) and, with
+    ``gate``, the output stage.  qp, kp, vp ``[B, n_tok, H, 128]`` bf16; z fp32 of the same
+    shape; a_log ``[H]``; b ``[B, n_tok, H]``.  Returns o ``[B, n_tok, H, 128]`` fp32."""
+    B, n_tok, H, d = qp.shape
+    _need(qp, "qp", torch.bfloat16)
+    _need(kp, "kp", torch.bfloat16, qp.shape)
+    _need(vp, "vp", torch.bfloat16, qp.shape)
+    _need(conv_w, "conv_w", torch.float32)
+    if conv_w.dim() != 4 or tuple(conv_w.shape[:3]) != (3, H, d):
+        raise ValueError(f"conv_w must have shape [3, {H}, {d}, W], got {tuple(conv_w.shape)}")
+    W = conv_w.shape[3]
+    if W > 1:
+        _need(conv_cache, "conv_cache", torch.float32, (B, H, 3, W - 1, d))
+    _need(z, "z", torch.float32, qp.shape)
+    _need(a_log, "a_log", torch.float32, (H,))
+    _need(b, "b", torch.float32, (B, n_tok, H))
+    _need(S_state, "S_state", torch.float32, (B, H, d, d))
+    if n_commit is not None:
+        _need(n_commit, "n_commit", torch.int32, (B,))
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, qp.shape)
+        if norm_weight is not None:
+            _need(norm_weight, "norm_weight", torch.float32, (d,))
+    if o is None:
+        o = torch.empty((B, n_tok, H, d), dtype=torch.float32, device=qp.device)
+    _need(o, "o", torch.float32, (B, n_tok, H, d))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    act = {"none": 0, "silu": 1}[conv_act]
+    st = library().kda_decode_fused(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(conv_w), _ptr(conv_cache) if W > 1 else None,
+                                    W, act, _ptr(z), _ptr(a_log), float(g_min), _ptr(b), _ptr(gate),
+                                    _ptr(norm_weight), float(eps), _ptr(S_state), _ptr(n_commit), _ptr(o), B, n_tok,
+                                    H, d, _ptr(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_decode_fused")
     return o
 
 

@@ -242,4 +242,34 @@ kda_status kda_decode_paged(const kda_bf16* q, const kda_bf16* k, const kda_bf16
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_decode_fused(const kda_bf16* qp, const kda_bf16* kp, const kda_bf16* vp, const float* conv_w,
+                            float* conv_cache, int conv_width, int conv_act, const float* z, const float* a_log,
+                            float g_min, const float* b, const kda_bf16* gate, const float* norm_weight, float eps,
+                            float* S_state, const int32_t* n_commit, float* o, int B, int n_tok, int H, int d,
+                            int* dev_status, cudaStream_t stream) {
+  if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (n_tok < 1 || n_tok > KDA_MAX_DECODE_TOKENS) return KDA_ERR_UNSUPPORTED;
+  if (conv_width < 1 || conv_width > kda::kMaxConvWidth) return KDA_ERR_UNSUPPORTED;
+  if (conv_act != 0 && conv_act != 1) return KDA_ERR_INVALID_ARG;
+  if (!(g_min < 0.f) || !std::isfinite(g_min)) return KDA_ERR_INVALID_ARG;
+  if (gate && (!(eps >= 0.f) || !std::isfinite(eps))) return KDA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return KDA_OK;
+  if (!qp || !kp || !vp || !conv_w || !z || !a_log || !b || !S_state || !o) return KDA_ERR_INVALID_ARG;
+  if (conv_width > 1 && !conv_cache) return KDA_ERR_INVALID_ARG;
+  if (!aligned(S_state, 16) || !aligned(o, 16) || !aligned(qp, 2) || !aligned(kp, 2) || !aligned(vp, 2) ||
+      !aligned(gate, 2) || !aligned(conv_w, 4) || !aligned(conv_cache, 4) || !aligned(z, 4) || !aligned(a_log, 4) ||
+      !aligned(b, 4) || !aligned(norm_weight, 4) || !aligned(n_commit, 4) || !aligned(dev_status, 4))
+    return KDA_ERR_ALIGNMENT;
+  kda_status st = current_device(nullptr);
+  if (st != KDA_OK) return st;
+  kda::FrontEnd fe;
+  fe.qp = qp; fe.kp = kp; fe.vp = vp; fe.conv_w = conv_w; fe.conv_cache = conv_cache; fe.W = conv_width;
+  fe.act = conv_act; fe.z = z; fe.a_log = a_log; fe.g_min = g_min; fe.b = b;
+  fe.gate = gate; fe.norm_weight = gate ? norm_weight : nullptr; fe.eps = gate ? eps : 0.f;
+  cudaError_t e = kda::launch_decode_fused(fe, S_state, n_commit, o, B, n_tok, H, dev_status, stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

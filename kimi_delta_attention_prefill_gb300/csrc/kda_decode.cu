@@ -20,6 +20,15 @@
 // there is no out table, no write for -1).  A destination other than the source always
 // receives the state after n_commit tokens, the entry state itself when n_commit = 0
 // (copy on write: a shared cached state is never modified).
+//
+// Fused front end (kda_decode_fused, "Kimi K3.1 Pro 架构完全拆解" 3.4: the replay kernel does
+// the short convolution, input normalisation, gating, recurrence and output normalisation;
+// the steps themselves follow "Kimi K3 ... 服務性能" section 7 and the K3.1 page 3.2): the
+// CTA stages the projected inputs of its head with the convolution cache, convolves each
+// channel (optional SiLU), L2-normalises q and k (one warp per row), forms
+// alpha = exp(g_min Sigmoid(e^A z)) and beta = Sigmoid(b), advances the cache by the
+// committed tokens, runs the same recurrence, and optionally applies the output stage
+// y = Sigmoid(gate) w o / sqrt(mean(o^2) + eps) before writing o.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -42,13 +51,80 @@ struct DecodeSmem {
   float beta[kMaxDecodeTokens];
   float kq[kMaxDecodeTokens];
 };
+template <bool kFront>
+struct DecodeSmemT : DecodeSmem {};
+template <>
+struct DecodeSmemT<true> : DecodeSmem {
+  float x[3][kMaxConvWidth - 1 + kMaxDecodeTokens][kD];  // convolution inputs: cache rows, then the tokens
+  float o[kMaxDecodeTokens][kD];                          // o before the output stage
+};
 
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+
+// Front end of one (sequence, head): projected inputs + cache -> sm.q, sm.k (unit rows),
+// sm.v, sm.alpha, sm.beta; the cache advanced by nc committed tokens (nc = 0: unchanged).
+__device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, int h, int H, int n_tok, int nc,
+                            int tid) {
+  const int Wm1 = fe.W - 1, rows = Wm1 + n_tok;
+  const int64_t cache_base = (static_cast<int64_t>(b) * H + h) * 3 * Wm1 * kD;
+  for (int e = tid; e < 3 * rows * kD; e += kThreads) {
+    const int s = e / (rows * kD), r = (e / kD) % rows, j = e % kD;
+    float x;
+    if (r < Wm1) {
+      x = fe.conv_cache[cache_base + (static_cast<int64_t>(s) * Wm1 + r) * kD + j];
+    } else {
+      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(s == 0 ? fe.qp : (s == 1 ? fe.kp : fe.vp));
+      x = __bfloat162float(src[((static_cast<int64_t>(b) * n_tok + (r - Wm1)) * H + h) * kD + j]);
+    }
+    sm.x[s][r][j] = x;
+  }
+  const float ea = expf(fe.a_log[h]);
+  for (int e = tid; e < n_tok * kD; e += kThreads) {
+    const int i = e / kD, j = e - i * kD;
+    const float zz = fe.z[((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + j];
+    sm.alpha[i][j] = expf(fe.g_min * sigmoidf_(ea * zz));
+  }
+  if (tid < n_tok) sm.beta[tid] = sigmoidf_(fe.b[(static_cast<int64_t>(b) * n_tok + tid) * H + h]);
+  __syncthreads();
+  // depthwise causal convolution: y_i = sum_t w[t] x_{i - t}
+  for (int e = tid; e < 3 * n_tok * kD; e += kThreads) {
+    const int s = e / (n_tok * kD), i = (e / kD) % n_tok, j = e % kD;
+    const float* wv = fe.conv_w + ((static_cast<int64_t>(s) * H + h) * kD + j) * fe.W;
+    float acc = 0.f;
+    for (int t = 0; t < fe.W; ++t) acc = fmaf(wv[t], sm.x[s][Wm1 + i - t][j], acc);
+    if (fe.act == 1) acc = acc * sigmoidf_(acc);
+    (s == 0 ? sm.q : (s == 1 ? sm.k : sm.v))[i][j] = acc;
+  }
+  __syncthreads();
+  // q and k rows to unit length (warps 0..n-1: q, 4..4+n-1: k); a zero row stays zero
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < n_tok || (warp >= 4 && warp < 4 + n_tok)) {
+    float* row = warp < 4 ? sm.q[warp] : sm.k[warp - 4];
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) ss = fmaf(row[lane + 32 * m], row[lane + 32 * m], ss);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float sc = ss > 0.f ? 1.f / sqrtf(ss) : 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) row[lane + 32 * m] *= sc;
+  }
+  // the cache after the committed tokens: rows [nc, nc + W - 1) of (cache, tokens)
+  if (nc > 0 && Wm1 > 0) {
+    for (int e = tid; e < 3 * Wm1 * kD; e += kThreads) {
+      const int s = e / (Wm1 * kD), r = (e / kD) % Wm1, j = e % kD;
+      fe.conv_cache[cache_base + (static_cast<int64_t>(s) * Wm1 + r) * kD + j] = sm.x[s][nc + r][j];
+    }
+  }
+}
+
+template <bool kFront>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
               const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
               float* __restrict__ S, const int32_t* __restrict__ n_commit, float* __restrict__ o, int n_tok,
-              int H, int* __restrict__ status, const PageTables pg) {
-  __shared__ DecodeSmem sm;
+              int H, int* __restrict__ status, const PageTables pg, const FrontEnd fe) {
+  __shared__ DecodeSmemT<kFront> sm;
   const int unit = blockIdx.x;  // b * H + h
   const int b = unit / H, h = unit - b * H;
   const int tid = threadIdx.x;
@@ -96,15 +172,19 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
   }
 
   // Stage this head's inputs for all tokens (tiny) while the state streams in.
-  for (int e = tid; e < n_tok * kD; e += kThreads) {
-    const int i = e / kD, j = e - i * kD;
-    const int64_t base = ((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + j;
-    sm.q[i][j] = __bfloat162float(q[base]);
-    sm.k[i][j] = __bfloat162float(k[base]);
-    sm.v[i][j] = __bfloat162float(v[base]);
-    sm.alpha[i][j] = expf(g[base]);
+  if constexpr (kFront) {
+    stage_front(sm, fe, b, h, H, n_tok, commit_ok ? nc : 0, tid);
+  } else {
+    for (int e = tid; e < n_tok * kD; e += kThreads) {
+      const int i = e / kD, j = e - i * kD;
+      const int64_t base = ((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + j;
+      sm.q[i][j] = __bfloat162float(q[base]);
+      sm.k[i][j] = __bfloat162float(k[base]);
+      sm.v[i][j] = __bfloat162float(v[base]);
+      sm.alpha[i][j] = expf(g[base]);
+    }
+    if (tid < n_tok) sm.beta[tid] = beta[(static_cast<int64_t>(b) * n_tok + tid) * H + h];
   }
-  if (tid < n_tok) sm.beta[tid] = beta[(static_cast<int64_t>(b) * n_tok + tid) * H + h];
   __syncthreads();
   if (warp < n_tok) {  // k . q of token `warp`
     float acc = 0.f;
@@ -140,8 +220,17 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     u.z = bt * (sm.v[i][col + 2] - w.z); u.w = bt * (sm.v[i][col + 3] - w.w);
     if (r0 == 0) {
       float4 ov = make_float4(p.x + u.x * kq, p.y + u.y * kq, p.z + u.z * kq, p.w + u.w * kq);
-      const int64_t ob = ((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + col;
-      *reinterpret_cast<float4*>(o + ob) = ov;
+      bool direct = true;
+      if constexpr (kFront) {
+        if (fe.gate) {  // normalised and gated after the loop
+          *reinterpret_cast<float4*>(&sm.o[i][col]) = ov;
+          direct = false;
+        }
+      }
+      if (direct) {
+        const int64_t ob = ((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + col;
+        *reinterpret_cast<float4*>(o + ob) = ov;
+      }
     }
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) {
@@ -153,6 +242,27 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
       for (int m = 0; m < kRowsPerThread; ++m) __stcs(&Sout[((r0 + 8 * m) * kD + col) >> 2], s[m]);
     }
   }
+  if constexpr (kFront) {
+    if (fe.gate) {  // output stage: warp i normalises and gates token i's row
+      __syncthreads();
+      if (warp < n_tok) {
+        const int64_t rb = ((static_cast<int64_t>(b) * n_tok + warp) * H + h) * kD;
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = fmaf(sm.o[warp][lane + 32 * m], sm.o[warp][lane + 32 * m], ss);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float sc = 1.f / sqrtf(ss * (1.f / kD) + fe.eps);
+        const __nv_bfloat16* gt = static_cast<const __nv_bfloat16*>(fe.gate) + rb;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int c = lane + 32 * m;
+          const float wgt = fe.norm_weight ? fe.norm_weight[c] : 1.f;
+          o[rb + c] = sigmoidf_(__bfloat162float(gt[c])) * wgt * sm.o[warp][c] * sc;
+        }
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -162,9 +272,18 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const flo
                           cudaStream_t stream, const PageTables& pages) {
   const int64_t units = static_cast<int64_t>(B) * H;
   if (units == 0) return cudaSuccess;
-  decode_kernel<<<static_cast<unsigned>(units), kThreads, 0, stream>>>(
+  decode_kernel<false><<<static_cast<unsigned>(units), kThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), g, beta, S, n_commit, o, n_tok, H, status, pages);
+      static_cast<const __nv_bfloat16*>(v), g, beta, S, n_commit, o, n_tok, H, status, pages, FrontEnd());
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fused(const FrontEnd& fe, float* S, const int32_t* n_commit, float* o, int B, int n_tok,
+                                int H, int* status, cudaStream_t stream) {
+  const int64_t units = static_cast<int64_t>(B) * H;
+  if (units == 0) return cudaSuccess;
+  decode_kernel<true><<<static_cast<unsigned>(units), kThreads, 0, stream>>>(
+      nullptr, nullptr, nullptr, nullptr, nullptr, S, n_commit, o, n_tok, H, status, PageTables(), fe);
   return cudaGetLastError();
 }
 

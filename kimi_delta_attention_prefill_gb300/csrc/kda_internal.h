@@ -39,9 +39,31 @@ __host__ inline size_t page_check_bytes(int64_t n_pages) { return 256 + 4 * stat
 cudaError_t launch_page_check(const int32_t* in, const int32_t* out, int64_t n_units, const int32_t* ckpt,
                               int64_t n_ckpt_entries, int64_t n_pages, void* ws, int* status, cudaStream_t stream);
 
+constexpr int kMaxConvWidth = 4;
+
+// Decode front end (kda_decode_fused): the step starts from projected inputs.
+struct FrontEnd {
+  const void* qp = nullptr;  // [B, n, H, d] bf16 projected inputs before the short convolution
+  const void* kp = nullptr;
+  const void* vp = nullptr;
+  const float* conv_w = nullptr;  // [3, H, d, W] depthwise filters of q, k, v (tap j: j steps back)
+  float* conv_cache = nullptr;    // [B, H, 3, W - 1, d] the W - 1 inputs before the step, oldest first
+  int W = 1;
+  int act = 0;                    // 0: none, 1: SiLU after the convolution
+  const float* z = nullptr;       // [B, n, H, d] decay-gate pre-activations
+  const float* a_log = nullptr;   // [H]
+  float g_min = -5.f;
+  const float* b = nullptr;       // [B, n, H] beta logits
+  const void* gate = nullptr;     // [B, n, H, d] bf16 output-gate logits, or nullptr
+  const float* norm_weight = nullptr;
+  float eps = 0.f;
+};
+
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, float* S,
                           const int32_t* n_commit, float* o, int B, int n_tok, int H, int* status,
                           cudaStream_t stream, const PageTables& pages = PageTables());
+cudaError_t launch_decode_fused(const FrontEnd& fe, float* S, const int32_t* n_commit, float* o, int B, int n_tok,
+                                int H, int* status, cudaStream_t stream);
 
 struct PrefillArgs {
   const void* q;

@@ -144,6 +144,48 @@ def make_output_stage(T, H, d=128, seed=0, device="cpu"):
     return gate, weight
 
 
+@dataclass
+class FrontEndInputs:
+    qp: torch.Tensor          # [B, n_tok, H, d] bf16 projected inputs
+    kp: torch.Tensor
+    vp: torch.Tensor
+    conv_w: torch.Tensor      # [3, H, d, W] fp32
+    conv_cache: torch.Tensor  # [B, H, 3, W - 1, d] fp32 (bf16-representable past inputs)
+    z: torch.Tensor           # [B, n_tok, H, d] fp32 decay-gate pre-activations
+    a_log: torch.Tensor       # [H] fp32
+    b: torch.Tensor           # [B, n_tok, H] fp32 beta logits
+    S0: torch.Tensor          # [B, H, d, d] fp32
+    n_commit: torch.Tensor | None
+    gate: torch.Tensor        # [B, n_tok, H, d] bf16 output-gate logits
+    norm_weight: torch.Tensor  # [d] fp32
+
+
+def make_decode_frontend(B, n_tok, H, W=4, d=128, seed=0, device="cpu", commit="all", s0_std=0.02):
+    """Inputs of a fused decode / verify step from projected inputs.  Draw order: qp, kp, vp,
+    conv filters, cache, z, a_log, b, S0, gate, norm weight; then n_commit (as make_decode).
+    qp, kp, vp ~ N(0, 1) -> bf16; filters ~ N(0, 0.5^2); the cache holds bf16-rounded N(0, 1)
+    past inputs; z ~ N(-4, 1) and a_log ~ N(0, 0.1^2), so that g = -5 Sigmoid(e^a z) is
+    typically about -0.09 like the other decode inputs; b ~ N(0, 1); S0 ~ N(0, s0_std^2)."""
+    gen = _gen(device, 31337 + seed)
+    rn = lambda *shape: torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    qp, kp, vp = (rn(B, n_tok, H, d).to(torch.bfloat16) for _ in range(3))
+    conv_w = rn(3, H, d, W) * 0.5
+    conv_cache = rn(B, H, 3, W - 1, d).to(torch.bfloat16).float()
+    z = rn(B, n_tok, H, d) - 4.0
+    a_log = rn(H) * 0.1
+    b = rn(B, n_tok, H)
+    S0 = rn(B, H, d, d) * s0_std
+    gate = rn(B, n_tok, H, d).to(torch.bfloat16)
+    norm_weight = 1.0 + 0.1 * rn(d)
+    n_commit = None
+    if commit == "random":
+        n_commit = torch.randint(0, n_tok + 1, (B,), generator=_gen("cpu", 7919 * seed + 3),
+                                 dtype=torch.int64).to(torch.int32)
+    elif commit != "all":
+        raise ValueError(commit)
+    return FrontEndInputs(qp, kp, vp, conv_w, conv_cache, z, a_log, b, S0, n_commit, gate, norm_weight)
+
+
 def make_page_tables(counts, n_pages, seed=0):
     """Distinct pages for several int32 page tables: ``counts`` entries each, drawn without
     replacement from a seeded permutation of ``range(n_pages)`` (scattered over the pool)."""

@@ -204,3 +204,30 @@ def test_paged_workspace_sizes(lib):
     assert kda.prefill_paged_workspace_size(1, 96, 8192, n_pages=10) == 256 + 40  # no split at 96 heads
     split = kda.prefill_workspace_size(4, 2, 10000, n_segments=3)
     assert kda.prefill_paged_workspace_size(4, 2, 10000, n_pages=7, n_segments=3) == (split + 255) // 256 * 256 + 284
+
+
+def _decode_fused(lib, W=4, act=0, g_min=-5.0, gate=None, eps=1e-5, cache=0x7000, n_tok=2, qp=0x1000, S=0x2000,
+                  B=2, H=2):
+    return lib.kda_decode_fused(P(qp) if qp else None, P(0x1100), P(0x1200), P(0x3000), P(cache) if cache else None,
+                                W, act, P(0x4000), P(0x5000), g_min, P(0x6000), P(gate) if gate else None, None, eps,
+                                P(S) if S else None, None, P(0x8000), B, n_tok, H, 128, None, None)
+
+
+def test_decode_fused_host_validation(lib):
+    """The fused decode front end ("Kimi K3.1 Pro 架构完全拆解" 3.4): widths, activation,
+    decay bound, epsilon and buffers are checked before any CUDA call."""
+    assert _decode_fused(lib, W=0) == UNSUPPORTED
+    assert _decode_fused(lib, W=5) == UNSUPPORTED
+    assert _decode_fused(lib, n_tok=5) == UNSUPPORTED
+    assert _decode_fused(lib, act=2) == INVALID
+    assert _decode_fused(lib, g_min=0.0) == INVALID
+    assert _decode_fused(lib, g_min=float("-inf")) == INVALID
+    assert _decode_fused(lib, gate=0x9000, eps=-1.0) == INVALID
+    assert _decode_fused(lib, cache=0) == INVALID       # W > 1 needs the cache
+    assert _decode_fused(lib, qp=0) == INVALID
+    assert _decode_fused(lib, S=0x2008) == ALIGNMENT
+    assert _decode_fused(lib, qp=0x1001) == ALIGNMENT
+    assert _decode_fused(lib, B=0) == OK
+    if not HAS_GPU:
+        assert _decode_fused(lib) in (CUDA, UNSUPPORTED)
+        assert _decode_fused(lib, W=1, cache=0) in (CUDA, UNSUPPORTED)
