@@ -335,6 +335,31 @@ def run_ours(args, world, rank, local):
                          "vs_contiguous": ms_local / ppms}}
     del pool
 
+    # fused front end (kda_decode_fused): the 256 x 96 verify step from projected inputs,
+    # 4 tokens with random commits, width-4 convolution with SiLU, output stage; algorithmic
+    # bytes per (sequence, head): the state read and write, per token the projected inputs
+    # (3 x 2d), z (4d), the beta logit, the gate logits (2d) and o (4d), and the
+    # convolution cache read and write (2 x 3 x (W - 1) x d x 4)
+    fx = inputs.make_decode_frontend(256, 4, H, W=4, seed=6, commit="random", device=dev)
+    fS = fx.S0.clone()
+    fcache = fx.conv_cache.clone()
+    fo = torch.empty((256, 4, H, D), dtype=torch.float32, device=dev)
+    fnc = fx.n_commit.to(dev)
+
+    def fstep():
+        kda.decode_fused(fx.qp, fx.kp, fx.vp, fx.conv_w, fcache, fx.z, fx.a_log, fx.b, fS, n_commit=fnc,
+                         conv_act="silu", gate=fx.gate, norm_weight=fx.norm_weight, o=fo, stream=stream)
+
+    fms = timed(fstep, dsteps)
+    f_bytes = n_units * (DECODE_STATE_BYTES + 4 * (3 * 2 * D + 4 * D + 4 + 2 * D + 4 * D) + 2 * 3 * 3 * D * 4)
+    fused = {"metric": "KDA fused verify step from projected inputs (256 x 96 heads, 4 tokens, random commits, "
+                       "conv width 4 + SiLU, L2 norm, gates, output stage), state GB/s",
+             "value": n_units * DECODE_STATE_BYTES / (fms / 1e3) / 1e9, "unit": "GB/s", "us_per_step": fms * 1e3,
+             "roofline": {"bound": "hbm", "achieved": f_bytes / (fms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": f_bytes / (fms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                          "kernel": "decode_kernel<front end>", "bytes_per_launch": f_bytes}}
+    del fx, fS, fcache, fo
+
     # end to end through the public call, host buffers: pinned H2D of the step's inputs,
     # the prefill, D2H of o and the final state
     hq, hk, hv, hg, hb = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta))
@@ -400,6 +425,7 @@ def run_ours(args, world, rank, local):
                                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes}},
             "gated": gated,
             "paged": paged,
+            "decode_fused": fused,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_prefill * args.steps,
             "clocks": clk.summary(),

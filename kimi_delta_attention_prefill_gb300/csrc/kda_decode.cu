@@ -24,8 +24,8 @@
 // Fused front end (kda_decode_fused, "Kimi K3.1 Pro 架构完全拆解" 3.4: the replay kernel does
 // the short convolution, input normalisation, gating, recurrence and output normalisation;
 // the steps themselves follow "Kimi K3 ... 服務性能" section 7 and the K3.1 page 3.2): the
-// CTA stages the projected inputs of its head with the convolution cache, convolves each
-// channel (optional SiLU), L2-normalises q and k (one warp per row), forms
+// CTA loads the projected inputs of its head with the convolution cache into registers,
+// convolves each channel (optional SiLU), L2-normalises q and k (one warp per row), forms
 // alpha = exp(g_min Sigmoid(e^A z)) and beta = Sigmoid(b), advances the cache by the
 // committed tokens, runs the same recurrence, and optionally applies the output stage
 // y = Sigmoid(gate) w o / sqrt(mean(o^2) + eps) before writing o.
@@ -55,66 +55,119 @@ template <bool kFront>
 struct DecodeSmemT : DecodeSmem {};
 template <>
 struct DecodeSmemT<true> : DecodeSmem {
-  float x[3][kMaxConvWidth - 1 + kMaxDecodeTokens][kD];  // convolution inputs: cache rows, then the tokens
-  float o[kMaxDecodeTokens][kD];                          // o before the output stage
+  float o[kMaxDecodeTokens][kD];   // o before the output stage
+  float gw[kMaxDecodeTokens][kD];  // output stage: Sigmoid(gate) x weight
 };
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
 // Front end of one (sequence, head): projected inputs + cache -> sm.q, sm.k (unit rows),
 // sm.v, sm.alpha, sm.beta; the cache advanced by nc committed tokens (nc = 0: unchanged).
+// Thread = channel j (tid mod d) of stream s = tid / d and, for the first half, also of
+// stream 2.  Its inputs sit right-aligned in a register window x[0..6]: token i at x[3 + i],
+// the cache's newest row at x[2], so tap t of token i reads x[3 + i - t] (a constant index);
+// every load of the thread is issued before the first use.
 __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, int h, int H, int n_tok, int nc,
                             int tid) {
-  const int Wm1 = fe.W - 1, rows = Wm1 + n_tok;
-  const int64_t cache_base = (static_cast<int64_t>(b) * H + h) * 3 * Wm1 * kD;
-  for (int e = tid; e < 3 * rows * kD; e += kThreads) {
-    const int s = e / (rows * kD), r = (e / kD) % rows, j = e % kD;
-    float x;
-    if (r < Wm1) {
-      x = fe.conv_cache[cache_base + (static_cast<int64_t>(s) * Wm1 + r) * kD + j];
-    } else {
-      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(s == 0 ? fe.qp : (s == 1 ? fe.kp : fe.vp));
-      x = __bfloat162float(src[((static_cast<int64_t>(b) * n_tok + (r - Wm1)) * H + h) * kD + j]);
-    }
-    sm.x[s][r][j] = x;
-  }
+  constexpr int kWin = kMaxConvWidth - 1 + kMaxDecodeTokens, kOff = kMaxConvWidth - 1;
+  const int W = fe.W, Wm1 = W - 1;
+  const int j = tid & (kD - 1), half = tid >> 7;
+  const int64_t cache_base = (static_cast<int64_t>(b) * H + h) * 3 * Wm1 * kD + j;
+  const int64_t tstride = static_cast<int64_t>(H) * kD;
+  const int64_t tok_base = static_cast<int64_t>(b) * n_tok * tstride + static_cast<int64_t>(h) * kD + j;
+  // gate inputs (independent of the convolution): tokens half and half + 2 of channel j
   const float ea = expf(fe.a_log[h]);
-  for (int e = tid; e < n_tok * kD; e += kThreads) {
-    const int i = e / kD, j = e - i * kD;
-    const float zz = fe.z[((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + j];
-    sm.alpha[i][j] = expf(fe.g_min * sigmoidf_(ea * zz));
-  }
-  if (tid < n_tok) sm.beta[tid] = sigmoidf_(fe.b[(static_cast<int64_t>(b) * n_tok + tid) * H + h]);
-  __syncthreads();
-  // depthwise causal convolution: y_i = sum_t w[t] x_{i - t}
-  for (int e = tid; e < 3 * n_tok * kD; e += kThreads) {
-    const int s = e / (n_tok * kD), i = (e / kD) % n_tok, j = e % kD;
-    const float* wv = fe.conv_w + ((static_cast<int64_t>(s) * H + h) * kD + j) * fe.W;
-    float acc = 0.f;
-    for (int t = 0; t < fe.W; ++t) acc = fmaf(wv[t], sm.x[s][Wm1 + i - t][j], acc);
-    if (fe.act == 1) acc = acc * sigmoidf_(acc);
-    (s == 0 ? sm.q : (s == 1 ? sm.k : sm.v))[i][j] = acc;
-  }
-  __syncthreads();
-  // q and k rows to unit length (warps 0..n-1: q, 4..4+n-1: k); a zero row stays zero
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp < n_tok || (warp >= 4 && warp < 4 + n_tok)) {
-    float* row = warp < 4 ? sm.q[warp] : sm.k[warp - 4];
-    float ss = 0.f;
+  float zz[2];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) ss = fmaf(row[lane + 32 * m], row[lane + 32 * m], ss);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float sc = ss > 0.f ? 1.f / sqrtf(ss) : 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) row[lane + 32 * m] *= sc;
+  for (int u = 0; u < 2; ++u) {
+    const int i = half + 2 * u;
+    zz[u] = i < n_tok ? fe.z[tok_base + i * tstride] : 0.f;
   }
-  // the cache after the committed tokens: rows [nc, nc + W - 1) of (cache, tokens)
-  if (nc > 0 && Wm1 > 0) {
-    for (int e = tid; e < 3 * Wm1 * kD; e += kThreads) {
-      const int s = e / (Wm1 * kD), r = (e / kD) % Wm1, j = e % kD;
-      fe.conv_cache[cache_base + (static_cast<int64_t>(s) * Wm1 + r) * kD + j] = sm.x[s][nc + r][j];
+  const float bl = tid < n_tok ? fe.b[(static_cast<int64_t>(b) * n_tok + tid) * H + h] : 0.f;
+  float ga[2] = {0.f, 0.f}, gwt = 1.f;  // output stage: gate logits of tokens half, half + 2; weight of j
+  if (fe.gate) {
+    const __nv_bfloat16* gt = static_cast<const __nv_bfloat16*>(fe.gate);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = half + 2 * u;
+      if (i < n_tok) ga[u] = __bfloat162float(gt[tok_base + i * tstride]);
     }
+    if (fe.norm_weight) gwt = fe.norm_weight[j];
+  }
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int s = half + 2 * pass;
+    if (s > 2) break;
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(s == 0 ? fe.qp : (s == 1 ? fe.kp : fe.vp));
+    float x[kWin];
+#pragma unroll
+    for (int r = 0; r < kWin; ++r) {
+      const int tau = r - kOff;  // token index; negative: the cache row Wm1 + tau
+      if (tau >= 0)
+        x[r] = tau < n_tok ? __bfloat162float(src[tok_base + tau * tstride]) : 0.f;
+      else
+        x[r] = Wm1 + tau >= 0 ? fe.conv_cache[cache_base + (static_cast<int64_t>(s) * Wm1 + Wm1 + tau) * kD] : 0.f;
+    }
+    float w[kMaxConvWidth];
+    const float* wv = fe.conv_w + ((static_cast<int64_t>(s) * H + h) * kD + j) * W;
+#pragma unroll
+    for (int t = 0; t < kMaxConvWidth; ++t) w[t] = t < W ? wv[t] : 0.f;
+    float* dst = s == 0 ? &sm.q[0][j] : (s == 1 ? &sm.k[0][j] : &sm.v[0][j]);
+#pragma unroll
+    for (int i = 0; i < kMaxDecodeTokens; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < kMaxConvWidth; ++t) acc = fmaf(w[t], x[kOff + i - t], acc);
+      if (fe.act == 1) acc = acc * sigmoidf_(acc);
+      if (i < n_tok) dst[i * kD] = acc;
+    }
+    // the cache after the committed tokens: full rows [nc, nc + Wm1), full row f = x[kOff - Wm1 + f]
+    if (nc > 0) {
+#pragma unroll
+      for (int rr = 0; rr < kMaxConvWidth - 1; ++rr) {
+        if (rr < Wm1) {
+          const int want = kOff - Wm1 + nc + rr;
+          float val = 0.f;
+#pragma unroll
+          for (int r = 0; r < kWin; ++r) val = r == want ? x[r] : val;
+          fe.conv_cache[cache_base + (static_cast<int64_t>(s) * Wm1 + rr) * kD] = val;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = half + 2 * u;
+    if (i < n_tok) {
+      sm.alpha[i][j] = expf(fe.g_min * sigmoidf_(ea * zz[u]));
+      if (fe.gate) sm.gw[i][j] = sigmoidf_(ga[u]) * gwt;
+    }
+  }
+  if (tid < n_tok) sm.beta[tid] = sigmoidf_(bl);
+  __syncthreads();
+  // warp i: q and k rows of token i to unit length (a zero row stays zero) and their dot
+  // product k . q for the recurrence, from one pass over the channels
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < n_tok) {
+    float qq = 0.f, kk = 0.f, kq = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float a = sm.q[warp][lane + 32 * m], c = sm.k[warp][lane + 32 * m];
+      qq = fmaf(a, a, qq); kk = fmaf(c, c, kk); kq = fmaf(a, c, kq);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      qq += __shfl_xor_sync(0xffffffffu, qq, off);
+      kk += __shfl_xor_sync(0xffffffffu, kk, off);
+      kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    }
+    const float sq = qq > 0.f ? 1.f / sqrtf(qq) : 0.f, sk = kk > 0.f ? 1.f / sqrtf(kk) : 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      sm.q[warp][lane + 32 * m] *= sq;
+      sm.k[warp][lane + 32 * m] *= sk;
+    }
+    if (lane == 0) sm.kq[warp] = kq * sq * sk;
   }
 }
 
@@ -186,15 +239,17 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     if (tid < n_tok) sm.beta[tid] = beta[(static_cast<int64_t>(b) * n_tok + tid) * H + h];
   }
   __syncthreads();
-  if (warp < n_tok) {  // k . q of token `warp`
-    float acc = 0.f;
+  if constexpr (!kFront) {
+    if (warp < n_tok) {  // k . q of token `warp` (the front end forms it with the normalisation)
+      float acc = 0.f;
 #pragma unroll
-    for (int j = lane; j < kD; j += 32) acc += sm.k[warp][j] * sm.q[warp][j];
+      for (int j = lane; j < kD; j += 32) acc += sm.k[warp][j] * sm.q[warp][j];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) sm.kq[warp] = acc;
+      for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) sm.kq[warp] = acc;
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   for (int i = 0; i < n_tok; ++i) {
     // X = Diag(alpha) S, then partial w = X^T k and p = X^T q over this thread's rows.
@@ -253,12 +308,10 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
 #pragma unroll
         for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float sc = 1.f / sqrtf(ss * (1.f / kD) + fe.eps);
-        const __nv_bfloat16* gt = static_cast<const __nv_bfloat16*>(fe.gate) + rb;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int c = lane + 32 * m;
-          const float wgt = fe.norm_weight ? fe.norm_weight[c] : 1.f;
-          o[rb + c] = sigmoidf_(__bfloat162float(gt[c])) * wgt * sm.o[warp][c] * sc;
+          o[rb + c] = sm.gw[warp][c] * sm.o[warp][c] * sc;
         }
       }
     }
