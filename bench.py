@@ -360,23 +360,19 @@ def run_ours(args, world, rank, local):
                           "kernel": "decode_kernel<front end>", "bytes_per_launch": f_bytes}}
     del fx, fS, fcache, fo
 
-    # end to end through the public call, host buffers: pinned H2D of the step's inputs,
-    # the prefill, D2H of o and the final state
+    # end to end through the public host-buffer call (kda_prefill_host): every step uploads
+    # its inputs from pinned host memory, computes, and downloads o and the final state;
+    # the call pipelines the three over blocks of the token stream
     hq, hk, hv, hg, hb = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta))
-    hcu = x.cu_seqlens.pin_memory()
+    hcu = x.cu_seqlens.to(torch.int32).contiguous().pin_memory()
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hS = torch.empty(S.shape, dtype=S.dtype).pin_memory()
-    dq, dk, dv, dg, db = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta))
-    dcu = torch.empty_like(cu)
+    hws = torch.empty(kda.prefill_host_workspace_size(1, H, T), dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hcu))
     d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
 
     def e2e_step():
-        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb), (dcu, hcu)):
-            dst.copy_(src, non_blocking=True)
-        kda.prefill(dq, dk, dv, dg, db, dcu, o=o, S_out=S, workspace=ws, stream=stream)
-        ho.copy_(o, non_blocking=True)
-        hS.copy_(S, non_blocking=True)
+        kda.prefill_host(hq, hk, hv, hg, hb, hcu, o=ho, S_out=hS, workspace=hws, stream=stream)
 
     for _ in range(2):
         e2e_step()

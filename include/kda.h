@@ -257,6 +257,44 @@ kda_status kda_decode_fused(const kda_bf16* qp, const kda_bf16* kp, const kda_bf
                             int* dev_status, cudaStream_t stream);
 
 /*
+ * kda_prefill_host -- kda_prefill from HOST buffers, with the transfers overlapped.
+ *
+ * The inputs and outputs live in host memory (pin them: cudaMemcpyAsync from pageable memory
+ * is not asynchronous).  The call cuts the packed token stream into blocks (borders on the
+ * chunk grid of the sequence they cut: a multiple of 64 tokens from its start) and pipelines
+ * them: block j + 1's rows of q, k, v, g, beta are uploaded while block j is computed on
+ * `stream` and block j - 1's rows of o are downloaded; the final states follow the last
+ * block.  Each block is an ordinary kda_prefill whose sequences start from the running
+ * states, updated in place in the workspace, so a sequence cut into blocks goes through
+ * exactly the chunks and fp32 states of one kda_prefill call (same bits whenever neither
+ * path splits a sequence into segments).  Not on the pages: an executor for callers whose
+ * tensors start on the host ("部署 Kimi K3 ..." section 1.1 motivates overlapping the
+ * transfers with the work).
+ *
+ *   q, k, v, g, beta, S_in (or NULL: zeros), cu_seqlens, o, S_out: as kda_prefill, in HOST
+ *                memory; cu_seqlens is read on the host to plan the blocks (a bad packing is
+ *                KDA_ERR_INVALID_ARG); no checkpoints
+ *   block_tokens 0: the library's choice (total_tokens / 8 rounded to 64, at least 1024);
+ *                else a multiple of 64.  At most 64 blocks (KDA_ERR_UNSUPPORTED beyond).
+ *   workspace    DEVICE memory of kda_prefill_host_workspace_size(...) bytes, 256-byte
+ *                aligned: device copies of the inputs, o and the states
+ * The call enqueues the work and returns: `stream` is made to wait for the last transfer, so
+ * synchronising it (or an event recorded on it) means o and S_out are in host memory.  The
+ * host buffers must stay valid until then.  Streams and events the call creates are released
+ * by the driver once the work has finished.
+ */
+size_t kda_prefill_host_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int64_t block_tokens);
+kda_status kda_prefill_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                            const float* beta, const float* S_in, const int32_t* cu_seqlens, int n_seq,
+                            int64_t total_tokens, kda_bf16* o, float* S_out, int H, int d, int64_t block_tokens,
+                            void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream);
+/* The block borders kda_prefill_host would use (host only, no CUDA call): writes up to
+ * max_borders of the n + 1 borders 0 = b_0 < ... < b_n = total_tokens and returns n (0 for
+ * no sequences), or -1 for a bad packing or block size, or more than 64 blocks. */
+int kda_prefill_host_blocks(const int32_t* cu_seqlens, int n_seq, int64_t total_tokens, int64_t block_tokens,
+                            int64_t* borders, int max_borders);
+
+/*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
  *
  * This entry point has no counterpart on the pages; it exists for the library's users.

@@ -82,6 +82,13 @@ def library():
             lib.kda_decode_fused.restype = _c_int
             lib.kda_decode_fused.argtypes = ([_vp] * 5 + [_c_int, _c_int] + [_vp, _vp, ctypes.c_float] + [_vp] * 3 +
                                              [ctypes.c_float] + [_vp] * 3 + [_c_int] * 4 + [_vp, _vp])
+            lib.kda_prefill_host_workspace_size.restype = _c_sz
+            lib.kda_prefill_host_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_i64, _c_i64]
+            lib.kda_prefill_host.restype = _c_int
+            lib.kda_prefill_host.argtypes = ([_vp] * 7 + [_c_int, _c_i64, _vp, _vp, _c_int, _c_int, _c_i64] +
+                                             [_vp, _c_sz, _vp, _vp])
+            lib.kda_prefill_host_blocks.restype = _c_int
+            lib.kda_prefill_host_blocks.argtypes = [_vp, _c_int, _c_i64, _c_i64, _vp, _c_int]
             lib.kda_prefill_noalloc.restype = _c_int
             lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                                 [_c_int, _c_int, _c_int, _vp, _vp])
@@ -367,6 +374,75 @@ def decode_paged(q, k, v, g, beta, state_pool, s_in_page, s_out_page=None, n_com
     if st != 0:
         raise KdaError(st, "kda_decode_paged")
     return o
+
+
+def _host(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def prefill_host_blocks(cu_seqlens, block_tokens=0):
+    """The block borders of :func:`prefill_host` for a host ``cu_seqlens`` (a list)."""
+    _host(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seq = cu_seqlens.shape[0] - 1
+    T = int(cu_seqlens[-1]) if n_seq >= 0 else 0
+    out = torch.zeros(66, dtype=torch.int64)
+    n = library().kda_prefill_host_blocks(_ptr(cu_seqlens), n_seq, T, int(block_tokens), _ptr(out), 66)
+    if n < 0:
+        raise ValueError("bad packing, block size, or more than 64 blocks")
+    return out[:n + 1].tolist() if n > 0 else []
+
+
+def prefill_host_workspace_size(n_seq, H, total_tokens, block_tokens=0, d=HEAD_DIM) -> int:
+    return int(library().kda_prefill_host_workspace_size(int(n_seq), int(H), int(d), int(total_tokens),
+                                                         int(block_tokens)))
+
+
+def prefill_host(q, k, v, g, beta, cu_seqlens, S_in=None, o=None, S_out=None, block_tokens=0, workspace=None,
+                 dev_status=None, stream=None):
+    """:func:`prefill` from host tensors (``kda_prefill_host``): uploads, computes and downloads
+    in pipelined blocks.  q, k, v, g, beta, S_in, o, S_out are HOST tensors (pinned for
+    overlap); cu_seqlens a host int32 tensor.  ``workspace`` is a device uint8 tensor (made
+    here when absent).  Returns ``(o, S_out)``; they are complete once ``stream`` is
+    synchronised."""
+    T, H, d = q.shape
+    _host(q, "q", torch.bfloat16)
+    _host(k, "k", torch.bfloat16, q.shape)
+    _host(v, "v", torch.bfloat16, q.shape)
+    _host(g, "g", torch.float32, q.shape)
+    _host(beta, "beta", torch.float32, (T, H))
+    _host(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seq = cu_seqlens.shape[0] - 1
+    if S_in is not None:
+        _host(S_in, "S_in", torch.float32, (n_seq, H, d, d))
+    if o is None:
+        o = torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory()
+    _host(o, "o", torch.bfloat16, (T, H, d))
+    if S_out is None:
+        S_out = torch.empty((n_seq, H, d, d), dtype=torch.float32).pin_memory()
+    _host(S_out, "S_out", torch.float32, (n_seq, H, d, d))
+    dev = torch.device("cuda", torch.cuda.current_device()) if stream is None else stream.device
+    if workspace is None:
+        workspace = torch.empty(prefill_host_workspace_size(n_seq, H, T, block_tokens, d), dtype=torch.uint8,
+                                device=dev)
+    _need(workspace, "workspace", torch.uint8)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_in), _ptr(cu_seqlens),
+                                    n_seq, T, _ptr(o), _ptr(S_out), H, d, int(block_tokens), _ptr(workspace),
+                                    workspace.numel(), _ptr(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_prefill_host")
+    return o, S_out
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -231,3 +231,20 @@ def test_decode_fused_host_validation(lib):
     if not HAS_GPU:
         assert _decode_fused(lib) in (CUDA, UNSUPPORTED)
         assert _decode_fused(lib, W=1, cache=0) in (CUDA, UNSUPPORTED)
+
+
+def test_prefill_from_host_buffers_validation(lib):
+    """kda_prefill_host reads the offsets on the host to plan its blocks: a bad packing or
+    block size is refused before any CUDA call."""
+    import numpy as np
+    cu = np.array([0, 64, 100], dtype=np.int32)
+    bad = np.array([0, 70, 60], dtype=np.int32)
+    f = lambda c, T=100, blk=0, ws=0x40000, wsb=1 << 30: lib.kda_prefill_host(
+        P(0x1000), P(0x1100), P(0x1200), P(0x1300), P(0x1400), None, c.ctypes.data, 2, T, P(0x1500), P(0x1600), 2,
+        128, blk, P(ws) if ws else None, wsb, None, None)
+    assert f(bad) == INVALID
+    assert f(cu, T=99) == INVALID          # cu[n] != total_tokens
+    assert f(cu, blk=100) == INVALID       # not a multiple of 64
+    assert f(cu, ws=0x40010) == ALIGNMENT
+    if not HAS_GPU:
+        assert f(cu) in (CUDA, UNSUPPORTED, WORKSPACE)
