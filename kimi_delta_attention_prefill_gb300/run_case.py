@@ -2,6 +2,8 @@
 
     python -m kimi_delta_attention_prefill_gb300.run_case --workload prefill_8k --heads 16 --iters 3
     python -m kimi_delta_attention_prefill_gb300.run_case --workload prefill_8k --gated   # + output stage
+    python -m kimi_delta_attention_prefill_gb300.run_case --workload verify --fused        # decode front end
+    python -m kimi_delta_attention_prefill_gb300.run_case --workload decode --paged        # states in pages
 
 Prints the mean CUDA-event time per call; exits non-zero if the library reports an error.
 """
@@ -23,6 +25,10 @@ def main():
     ap.add_argument("--segments", type=int, default=0, help="prefill segment count (0 = library's choice)")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--gated", action="store_true", help="prefill with the fused output stage")
+    ap.add_argument("--fused", action="store_true",
+                    help="decode from projected inputs (kda_decode_fused: width-4 conv + SiLU, output stage)")
+    ap.add_argument("--paged", action="store_true",
+                    help="decode with the states scattered in a page pool (kda_decode_paged, copy to fresh pages)")
     args = ap.parse_args()
     over = {}
     if args.heads:
@@ -34,7 +40,25 @@ def main():
     if inputs.WORKLOADS[args.workload]["kind"] == "decode":
         S = x.S0.clone()
         nc = None if x.n_commit is None else x.n_commit.cuda()
-        run = lambda: kda.decode(x.q, x.k, x.v, x.g, x.beta, S, n_commit=nc, dev_status=status)
+        B, n_tok, H = x.q.shape[0], x.q.shape[1], x.q.shape[2]
+        if args.fused:
+            w = inputs.WORKLOADS[args.workload]
+            fx = inputs.make_decode_frontend(B, n_tok, H, W=4, seed=w["seed"], device="cuda",
+                                             commit=w.get("commit", "all"))
+            fS, fc = fx.S0.clone(), fx.conv_cache.clone()
+            fnc = None if fx.n_commit is None else fx.n_commit.cuda()
+            run = lambda: kda.decode_fused(fx.qp, fx.kp, fx.vp, fx.conv_w, fc, fx.z, fx.a_log, fx.b, fS, n_commit=fnc,
+                                           conv_act="silu", gate=fx.gate, norm_weight=fx.norm_weight,
+                                           dev_status=status)
+        elif args.paged:
+            n_units = B * H
+            pin, pout = inputs.make_page_tables([n_units, n_units], 2 * n_units + 1024, seed=5)
+            pool = torch.zeros((2 * n_units + 1024, 128, 128), dtype=torch.float32, device="cuda")
+            pool[pin.long().cuda()] = x.S0.reshape(-1, 128, 128)
+            pin, pout = pin.cuda(), pout.cuda()
+            run = lambda: kda.decode_paged(x.q, x.k, x.v, x.g, x.beta, pool, pin, pout, n_commit=nc, dev_status=status)
+        else:
+            run = lambda: kda.decode(x.q, x.k, x.v, x.g, x.beta, S, n_commit=nc, dev_status=status)
     else:
         cu = x.cu_seqlens.cuda()
         off = None if x.ckpt_off is None else x.ckpt_off.cuda()
