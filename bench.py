@@ -335,6 +335,29 @@ def run_ours(args, world, rank, local):
                          "vs_contiguous": ms_local / ppms}}
     del pool
 
+    # the 1M-token, 8-head prefill: the planner splits each head's sequence over the SMs
+    # (per-segment (M, S~), scan of the entry states, second pass); its roofline is the same
+    # algorithmic bytes per token-head as the 8K launch
+    mx = inputs.make_workload("prefill_1m", device=dev)
+    mT, mH = mx.q.shape[0], mx.q.shape[1]
+    mcu = mx.cu_seqlens.to(dev)
+    mo = torch.empty_like(mx.q)
+    mS = torch.empty((1, mH, D, D), dtype=torch.float32, device=dev)
+    mws = torch.empty(max(kda.prefill_workspace_size(1, mH, mT), 1), dtype=torch.uint8, device=dev)
+
+    def mstep():
+        kda.prefill(mx.q, mx.k, mx.v, mx.g, mx.beta, mcu, o=mo, S_out=mS, workspace=mws, stream=stream)
+
+    mms = timed(mstep, 5)
+    m_bytes = mT * mH * PREFILL_BYTES_PER_TOKEN_HEAD + mH * STATE_BYTES
+    long_prefill = {"metric": "KDA prefill tokens/s (1 x 1,048,576 tokens, H=8, d=128, SM-level sequence split)",
+                    "value": mT / (mms / 1e3), "unit": "tokens/s", "ms_per_step": mms,
+                    "roofline": {"bound": "hbm", "achieved": m_bytes / (mms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": m_bytes / (mms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                 "traffic": None, "kernel": "prefill_kernel (split: pass 1, scan, pass 3)",
+                                 "bytes_per_launch": m_bytes}}
+    del mx, mo, mS, mws
+
     # fused front end (kda_decode_fused): the 256 x 96 verify step from projected inputs,
     # 4 tokens with random commits, width-4 convolution with SiLU, output stage; algorithmic
     # bytes per (sequence, head): the state read and write, per token the projected inputs
@@ -422,6 +445,7 @@ def run_ours(args, world, rank, local):
             "gated": gated,
             "paged": paged,
             "decode_fused": fused,
+            "prefill_1m": long_prefill,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_prefill * args.steps,
             "clocks": clk.summary(),
