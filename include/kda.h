@@ -295,6 +295,19 @@ int kda_prefill_host_blocks(const int32_t* cu_seqlens, int n_seq, int64_t total_
                             int64_t* borders, int max_borders);
 
 /*
+ * kda_debug_stall_next_prefill -- test hook for the bounded waits (no counterpart on the
+ * pages).  The next prefill launch of this process runs a test instance of the kernel
+ * whose prep warps withhold their first hand-off of chunk `chunk` (counted within each
+ * work item) and whose waits give up after 4096 polls.  The recurrence's wait for that
+ * hand-off then runs out: both warp groups leave their loops together, the copies and
+ * tensor-core products still in flight land (bounded), the tensor memory is released, and
+ * KDA_ERR_TIMEOUT is written to dev_status; that call's outputs are undefined.  Nothing
+ * faults or traps and the CUDA context stays usable.  Host side only; one-shot.  (The
+ * production instance's waits give up after 2^26 polls.)
+ */
+void kda_debug_stall_next_prefill(int chunk);
+
+/*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
  *
  * This entry point has no counterpart on the pages; it exists for the library's users.

@@ -89,6 +89,9 @@ def library():
                                              [_vp, _c_sz, _vp, _vp])
             lib.kda_prefill_host_blocks.restype = _c_int
             lib.kda_prefill_host_blocks.argtypes = [_vp, _c_int, _c_i64, _c_i64, _vp, _c_int]
+            if hasattr(lib, "kda_debug_stall_next_prefill"):  # diagnostic hook (tests)
+                lib.kda_debug_stall_next_prefill.restype = None
+                lib.kda_debug_stall_next_prefill.argtypes = [_c_int]
             lib.kda_prefill_noalloc.restype = _c_int
             lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                                 [_c_int, _c_int, _c_int, _vp, _vp])
@@ -443,6 +446,13 @@ def prefill_host(q, k, v, g, beta, cu_seqlens, S_in=None, o=None, S_out=None, bl
     if st != 0:
         raise KdaError(st, "kda_prefill_host")
     return o, S_out
+
+
+def debug_stall_next_prefill(chunk):
+    """Test hook (``kda_debug_stall_next_prefill``): the next prefill launch withholds one
+    hand-off at ``chunk`` and gives up its waits after 4096 polls, so it reports
+    KDA_ERR_TIMEOUT in ``dev_status`` without any fault."""
+    library().kda_debug_stall_next_prefill(int(chunk))
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -40,6 +40,9 @@ kda_status current_device(int* sms) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// kda_debug_stall_next_prefill: consumed by the next prefill launch
+std::atomic<int> g_stall_chunk{-1};
+
 }  // namespace
 
 extern "C" {
@@ -138,6 +141,7 @@ kda_status prefill_impl(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
   a.o = o; a.S_out = S_out; a.ckpts = ckpts; a.H = H; a.n_segments = n_segments;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = dev_status; a.stream = stream;
   a.gate = gate; a.norm_weight = norm_weight; a.eps = eps;
+  if (g_stall_chunk.load(std::memory_order_relaxed) >= 0) a.stall_chunk = g_stall_chunk.exchange(-1);
   if (pages) {
     void* pws = static_cast<uint8_t*>(workspace) + up256(split);
     a.pages = *pages;
@@ -178,6 +182,8 @@ kda_status kda_prefill_gated(const kda_bf16* q, const kda_bf16* k, const kda_bf1
                       ckpt_pos, n_ckpt, y, S_out, ckpts, H, d, n_segments, workspace, workspace_bytes, dev_status,
                       stream);
 }
+
+void kda_debug_stall_next_prefill(int chunk) { g_stall_chunk.store(chunk < 0 ? -1 : chunk); }
 
 size_t kda_prefill_paged_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int n_segments,
                                         int64_t n_pages) {

@@ -86,6 +86,7 @@ struct PrefillArgs {
   float* S_out;
   float* ckpts;
   PageTables pages;  // paged S_in / S_out / checkpoints when pages.pool is set
+  int stall_chunk = -1;  // test hook (kda_debug_stall_next_prefill): a withheld hand-off
   int H;
   int n_segments;  // 0 = planner, k >= 1 forced
   void* workspace;

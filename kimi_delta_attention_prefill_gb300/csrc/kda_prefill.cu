@@ -136,6 +136,7 @@ struct KParams {
   float* ckpts;
   PageTables pg;  // paged S_in / S_out / checkpoints when pg.pool is set
   int* status;
+  int stall_chunk;  // test hook (kernel instance kHook only): the prep group withholds this chunk's first hand-off
   int n_seq, H;
   int64_t total_tokens;
   int64_t n_ckpt;
@@ -182,6 +183,16 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
     }
   }
   return true;
+}
+
+// The kernel's waits, all bounded.  The instance kHook (launched only by the test hook
+// kda_debug_stall_next_prefill) gives up after 4096 polls so that a withheld hand-off
+// ends the launch quickly; the production instance keeps mbar_wait's default limit (its
+// polling loop, a compile-time bound, measurably shapes this latency-bound kernel's code).
+template <bool kHook>
+__device__ __forceinline__ bool kwait(uint64_t* bar, uint32_t parity) {
+  if constexpr (kHook) return mbar_wait(bar, parity, 4096u);
+  else return mbar_wait(bar, parity);
 }
 
 // Paged mode: every page a work item may touch lies in [-1, n_pages).
@@ -377,6 +388,7 @@ __device__ __forceinline__ void issue_qk(const KParams& p, const Work& w, uint8_
 // Gx[tb] = G[16 tb - 1] (0 for tb = 0): the row side e^{G[t] - Gx[tb(t)]} is <= 1 and the
 // column side e^{Gx[tb] - G[s]} is <= e^{16 x 5} = e^80 for s in the block (the pages'
 // 16-token bound), <= 1 for earlier s.
+template <bool kHook>
 __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                            uint32_t tmem, int n_chunks, int ptid) {
   // Registers: the launch gives every thread 168; the recurrent group gives some back
@@ -426,7 +438,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     //         tokens, warp scan over the block's 4 quads.  The block's total decay
     //         A[tb] = 2^(block sum) goes to shared memory for the other blocks' factors.
     float G[4][8];
-    if (!mbar_wait(&bars[BAR_G], n & 1)) ctrl[CTRL_ABORT] = 1;
+    if (!kwait<kHook>(&bars[BAR_G], n & 1)) ctrl[CTRL_ABORT] = 1;
     {
       const int valid_g = min(kChunk, w.len - cidx * kChunk);
       const float* gt = reinterpret_cast<const float*>(sm + SM_QAKA);  // [64][128] fp32
@@ -486,7 +498,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
       float al[8];
       // raw q, k of this thread's tokens (TMA, in the [K_decay; Q_decay] buffer): issued
       // now so their latency overlaps the factor products
-      if (!mbar_wait(&bars[BAR_QK], n & 1)) ctrl[CTRL_ABORT] = 1;
+      if (!kwait<kHook>(&bars[BAR_QK], n & 1)) ctrl[CTRL_ABORT] = 1;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint8_t* kqp = sm + SM_KQ + kpanel * 16384;
@@ -604,7 +616,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     fence_proxy_async_smem();
     named_bar_sync(kBarP, kPThreads);
     if (ptid == 0) {
-      mbar_arrive(&bars[BAR_KQ]);  // [K_decay; Q_decay] and a_last of this chunk are in place
+      if (!kHook || n != p.stall_chunk) mbar_arrive(&bars[BAR_KQ]);  // [K_decay; Q_decay] and a_last of this chunk are in place
       tc_fence_after();            // L and M_qk: one M = 128, N = 160 product
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -615,10 +627,10 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
 
     // ---- 4. L (fp32, beta-scaled) and M_qk (fp16, straight into rows 64..127 of the
     //         [INV Diag(beta); M_qk] operand, once the previous chunk's update is done)
-    if (!mbar_wait(&bars[BAR_LM], n & 1)) ctrl[CTRL_ABORT] = 1;
+    if (!kwait<kHook>(&bars[BAR_LM], n & 1)) ctrl[CTRL_ABORT] = 1;
     tc_fence_after();
     if (ptid == 0 && has_next) issue_g(cidx + 1);  // QA / KA consumed: the region takes the next g
-    if (n > 0 && !mbar_wait(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
+    if (n > 0 && !kwait<kHook>(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
     {
       const int q = pw & 3, part = pw >> 2;  // TMEM lane quarter; two warps split its columns
       const bool is_l = q >= 2;
@@ -677,9 +689,11 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     for (int u = 0; u < 4; ++u)
       st4(sm + SM_KR + kpanel * 8192 + sw128(t0 + u, 16 * kchunk), krq[u][0], krq[u][1], krq[u][2], krq[u][3]);
     fence_proxy_async_smem();
-    named_bar_sync(kBarP, kPThreads);
+    // one decision for the whole group: a thread that saw the abort flag later than another
+    // must not stay behind at the next barrier
+    const bool abort = named_bar_any(kBarP, kPThreads, ctrl[CTRL_ABORT] != 0);
     if (ptid == 0) { mbar_arrive(&bars[BAR_IM]); mbar_arrive(&bars[BAR_KR]); }
-    if (ctrl[CTRL_ABORT]) break;
+    if (abort) break;
   }
 }
 
@@ -721,6 +735,7 @@ __device__ __forceinline__ void sigmoid_w_half2(const uint4& a8, const uint32_t 
 // 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (P, then U)
 // belong to warps 0-1, rows 64-127 (Q_decay S, then O) to warps 2-3; the state TS uses
 // all 128 lanes.
+template <bool kHook>
 __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                                 uint32_t tmem, int n_chunks, bool do_o, bool v_zero, bool entry_identity, int tid) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
@@ -757,7 +772,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
           pack_half2(r[8 * c + 4], r[8 * c + 5]), pack_half2(r[8 * c + 6], r[8 * c + 7]));
     // TMEM holds the state already decayed by the first chunk's a_last (the update adds
     // K_restore^T U to Diag(a_last) S); the fp16 operand keeps the entry state itself.
-    if (g == 0 && !mbar_wait(&bars[BAR_AL], 0)) ctrl[CTRL_ABORT] = 1;
+    if (g == 0 && !kwait<kHook>(&bars[BAR_AL], 0)) ctrl[CTRL_ABORT] = 1;
     const float al0 = alast[i];
 #pragma unroll
     for (int e = 0; e < 32; ++e) r[e] *= al0;
@@ -798,7 +813,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     }
 
     // ---- P = K_decay S, Q_decay S (one M = 128 product)
-    if (!mbar_wait(&bars[BAR_KQ], n & 1)) ctrl[CTRL_ABORT] = 1;
+    if (!kwait<kHook>(&bars[BAR_KQ], n & 1)) ctrl[CTRL_ABORT] = 1;
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -810,7 +825,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     // ---- X = V - P (rows past the sequence end are zero)
     //      Warps 0-1 own rows 0-63 (P, X, U); warps 2-3 meanwhile prepare the output stage.
     if (rw < 2) {
-      if (!mbar_wait(&bars[BAR_M1], n & 1) || !mbar_wait(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
+      if (!kwait<kHook>(&bars[BAR_M1], n & 1) || !kwait<kHook>(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
       if (tid == 0 && n + 1 < n_chunks) issue_qk(p, w, sm, bars, cidx + 1);  // the buffer is free again
       {
@@ -841,7 +856,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
 
       // ---- U = INV Diag(beta) X (lanes 64-127 keep Q_decay S)
       if (tid == 0) {
-        if (!mbar_wait(&bars[BAR_IM], n & 1)) ctrl[CTRL_ABORT] = 1;
+        if (!kwait<kHook>(&bars[BAR_IM], n & 1)) ctrl[CTRL_ABORT] = 1;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -849,7 +864,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
                          0xffffffffu, 0xffffffffu);
         mma_commit(&bars[BAR_M2]);
       }
-      if (!mbar_wait(&bars[BAR_M2], n & 1)) ctrl[CTRL_ABORT] = 1;
+      if (!kwait<kHook>(&bars[BAR_M2], n & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
       {
         const int t = tid;
@@ -874,7 +889,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
 
       // ---- S += K_restore^T U ; O += M_qk U (lanes 0-63 untouched)
       if (tid == 0) {
-        if (!mbar_wait(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
+        if (!kwait<kHook>(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -912,7 +927,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       }
       tmem_wait_st();
     }
-    if (!mbar_wait(&bars[BAR_M34], n & 1)) ctrl[CTRL_ABORT] = 1;
+    if (!kwait<kHook>(&bars[BAR_M34], n & 1)) ctrl[CTRL_ABORT] = 1;
     tc_fence_after();
     // ---- outputs (rows in lanes 64-127)
     if (do_o && rw >= 2 && !gated) {
@@ -977,7 +992,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       const bool next = n + 1 < n_chunks;
       float al_next = 1.f;
       if (next) {
-        if (!mbar_wait(&bars[BAR_AL], (n + 1) & 1)) ctrl[CTRL_ABORT] = 1;
+        if (!kwait<kHook>(&bars[BAR_AL], (n + 1) & 1)) ctrl[CTRL_ABORT] = 1;
         al_next = alast[((n + 1) & 1) * 128 + i];
       }
       const int pos = min((cidx + 1) * kChunk, w.len);
@@ -1018,11 +1033,11 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    named_bar_sync(kBarR, kRThreads);
-    if (ctrl[CTRL_ABORT]) break;
+    if (named_bar_any(kBarR, kRThreads, ctrl[CTRL_ABORT] != 0)) break;  // one decision for the group
   }
 }
 
+template <bool kHook>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1110,9 +1125,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int n_chunks = w.c1 - w.c0;
 
   if (tid < kRThreads)
-    recurrent_group(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
+    recurrent_group<kHook>(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
   else
-    prep_group(p, w, sm, bars, ctrl, tmem, n_chunks, tid - kRThreads);
+    prep_group<kHook>(p, w, sm, bars, ctrl, tmem, n_chunks, tid - kRThreads);
 
   __syncthreads();
   if (ctrl[CTRL_ABORT]) {
@@ -1176,18 +1191,22 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.o = static_cast<__nv_bfloat16*>(a.o); p.S_out = a.S_out; p.ckpts = a.ckpts; p.status = a.status;
   p.gate = static_cast<const __nv_bfloat16*>(a.gate); p.norm_weight = a.norm_weight; p.eps = a.eps;
   p.pg = a.pages;
+  p.stall_chunk = a.stall_chunk;
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  // the test hook's instance only when kda_debug_stall_next_prefill armed this launch
+  auto kernel = a.stall_chunk >= 0 ? prefill_kernel<true> : prefill_kernel<false>;
   const SplitLayout L = split_layout(a.n_seq, a.H, T, a.n_segments, num_sms);
   if (L.extra == 0) {
     // one CTA per (sequence, head), whole sequence
-    prefill_kernel<<<dim3(static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
-                     a.stream>>>(p);
+    kernel<<<dim3(static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
     return cudaGetLastError();
   }
   // sequence split: plan, pass 1 (first segments + (S~, M) of middle segments), scan, pass 3
@@ -1197,14 +1216,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.slots = reinterpret_cast<float*>(ws + L.off_slots);
   p.items = reinterpret_cast<const int4*>(ws + L.off_items1);
   p.item_count = reinterpret_cast<const int*>(ws);
-  prefill_kernel<<<dim3(static_cast<unsigned>(L.max1), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
-                   a.stream>>>(p);
+  kernel<<<dim3(static_cast<unsigned>(L.max1), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_split_scan(a, L)) != cudaSuccess) return e;
   p.items = reinterpret_cast<const int4*>(ws + L.off_items3);
   p.item_count = reinterpret_cast<const int*>(ws) + 1;
-  prefill_kernel<<<dim3(static_cast<unsigned>(L.max3), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
-                   a.stream>>>(p);
+  kernel<<<dim3(static_cast<unsigned>(L.max3), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
   return cudaGetLastError();
 }
 

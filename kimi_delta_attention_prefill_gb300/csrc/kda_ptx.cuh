@@ -100,6 +100,21 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.L2 [%0];\n" ::"l"(reinterpret_cast<uint64_t>(ptr)));
 }
 
+// Named barrier over `count` threads that also ORs `pred` over them: every participant gets
+// the same answer (a group-wide decision no thread can see differently).
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
