@@ -41,6 +41,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -1193,13 +1194,17 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.pg = a.pages;
   p.stall_chunk = a.stall_chunk;
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory opt-in is a per-device attribute of the function: set it once per device
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(bit, std::memory_order_release);
   }
   // the test hook's instance only when kda_debug_stall_next_prefill armed this launch
   auto kernel = a.stall_chunk >= 0 ? prefill_kernel<true> : prefill_kernel<false>;
