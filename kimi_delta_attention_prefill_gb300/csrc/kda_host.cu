@@ -238,20 +238,29 @@ kda_status kda_prefill_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16
   for (int j = 0; j < tab.n; ++j)
     if (own.event(&landed[j]) != cudaSuccess || own.event(&computed[j]) != cudaSuccess) return KDA_ERR_CUDA;
 
+  // On a failure after the first enqueue, the work already queued on the two internal
+  // streams may still run: the caller's stream is made to wait for it before returning, so
+  // that synchronising `stream` still means no transfer touches the caller's buffers.
+  auto fail = [&](kda_status code) {
+    cudaEvent_t e;
+    for (cudaStream_t sx : {up, down})
+      if (own.event(&e) == cudaSuccess && cudaEventRecord(e, sx) == cudaSuccess) cudaStreamWaitEvent(stream, e, 0);
+    return code;
+  };
   const size_t HD = static_cast<size_t>(H) * kHeadDim;
   const size_t state_bytes = static_cast<size_t>(n_seq) * HD * kHeadDim * sizeof(float);
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
   // the workspace may still be in use by the caller's earlier work
   if (!ok(cudaEventRecord(start, stream)) || !ok(cudaStreamWaitEvent(up, start, 0)) ||
       !ok(cudaStreamWaitEvent(down, start, 0)))
-    return KDA_ERR_CUDA;
+    return fail(KDA_ERR_CUDA);
   if (!ok(cudaMemcpyAsync(d_cu, cu_seqlens, 4 * static_cast<size_t>(n_seq + 1), cudaMemcpyHostToDevice, up)))
-    return KDA_ERR_CUDA;
+    return fail(KDA_ERR_CUDA);
   block_cu_kernel<<<tab.n, 128, 0, up>>>(d_cu, tab, d_bcu);
-  if (!ok(cudaGetLastError())) return KDA_ERR_CUDA;
+  if (!ok(cudaGetLastError())) return fail(KDA_ERR_CUDA);
   if (!ok(S_in ? cudaMemcpyAsync(d_S, S_in, state_bytes, cudaMemcpyHostToDevice, up)
                : cudaMemsetAsync(d_S, 0, state_bytes, up)))
-    return KDA_ERR_CUDA;
+    return fail(KDA_ERR_CUDA);
   for (int j = 0; j < tab.n; ++j) {
     const HostBlock& b = tab.blk[j];
     const size_t r0 = static_cast<size_t>(b.a), nr = static_cast<size_t>(b.e - b.a);
@@ -262,9 +271,9 @@ kda_status kda_prefill_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16
           !ok(cudaMemcpyAsync(d_v + e2, v + e2, 2 * n2, cudaMemcpyHostToDevice, up)) ||
           !ok(cudaMemcpyAsync(d_g + e2, g + e2, 4 * n2, cudaMemcpyHostToDevice, up)) ||
           !ok(cudaMemcpyAsync(d_beta + r0 * H, beta + r0 * H, 4 * nr * H, cudaMemcpyHostToDevice, up)))
-        return KDA_ERR_CUDA;
+        return fail(KDA_ERR_CUDA);
     }
-    if (!ok(cudaEventRecord(landed[j], up)) || !ok(cudaStreamWaitEvent(stream, landed[j], 0))) return KDA_ERR_CUDA;
+    if (!ok(cudaEventRecord(landed[j], up)) || !ok(cudaStreamWaitEvent(stream, landed[j], 0))) return fail(KDA_ERR_CUDA);
     // block j: its sequences start from (and end in) the running states, in place
     float* Sj = d_S + static_cast<size_t>(b.s0) * HD * kHeadDim;
     const size_t e2 = r0 * HD;
@@ -272,15 +281,15 @@ kda_status kda_prefill_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16
         kda_prefill(d_q + e2, d_k + e2, d_v + e2, d_g + e2, d_beta + r0 * H, Sj, d_bcu + tab.cu_off[j],
                     b.s1 - b.s0, b.e - b.a, nullptr, nullptr, 0, d_o + e2, Sj, nullptr, H, d, 0, d_split, split,
                     dev_status, stream);
-    if (st != KDA_OK) return st;
+    if (st != KDA_OK) return fail(st);
     if (!ok(cudaEventRecord(computed[j], stream)) || !ok(cudaStreamWaitEvent(down, computed[j], 0)))
-      return KDA_ERR_CUDA;
+      return fail(KDA_ERR_CUDA);
     if (nr > 0 && !ok(cudaMemcpyAsync(o + e2, d_o + e2, 2 * nr * HD, cudaMemcpyDeviceToHost, down)))
-      return KDA_ERR_CUDA;
+      return fail(KDA_ERR_CUDA);
   }
   if (!ok(cudaMemcpyAsync(S_out, d_S, state_bytes, cudaMemcpyDeviceToHost, down)) ||
       !ok(cudaEventRecord(done, down)) || !ok(cudaStreamWaitEvent(stream, done, 0)))
-    return KDA_ERR_CUDA;
+    return fail(KDA_ERR_CUDA);
   return KDA_OK;
 }
 
