@@ -307,3 +307,38 @@ def test_decode_page_violations_write_nothing(bad):
     torch.cuda.synchronize()
     assert int(st.item()) == DEVICE_CHECK
     assert torch.isnan(o).all() and torch.equal(pool, before)
+
+
+def test_decode_paged_mixed_tables():
+    """Copy to fresh pages for some units, in place for others (out = in), -1 entries for a
+    zero entry state and for no write, n_commit random: each unit as the contiguous call."""
+    B, H = 4, 2
+    x, d = decode_case(B, 4, H, seed=86, commit="random")
+    s_in = torch.tensor([0, -1, 2, 3, 4, -1, 6, 7], dtype=torch.int32)
+    s_out = torch.tensor([10, 11, 2, -1, 14, -1, 6, 17], dtype=torch.int32)
+    pool = canary_pool(20, 11)
+    S0 = torch.zeros(B * H, 128, 128, device="cuda")
+    for u, pg in enumerate(s_in.tolist()):
+        if pg >= 0:
+            S0[u] = pool[pg]
+    d["S0"] = S0.reshape(B, H, 128, 128)
+    before = pool.clone()
+    o_ref, S_ref = contiguous_decode(d)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = kda.decode_paged(d["q"], d["k"], d["v"], d["g"], d["beta"], pool, s_in.cuda(), s_out.cuda(),
+                         n_commit=d["n_commit"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(o, o_ref)
+    flat = S_ref.reshape(-1, 128, 128)
+    nc = x.n_commit.tolist()
+    written = set()
+    for u, (pi, po) in enumerate(zip(s_in.tolist(), s_out.tolist())):
+        if po < 0:
+            continue
+        written.add(po)
+        if po == pi and nc[u // H] == 0:
+            assert torch.equal(pool[po], before[po])  # in place, nothing committed: untouched
+        else:
+            assert torch.equal(pool[po], flat[u])     # a fresh page always takes the committed state
+    keep = [p for p in range(20) if p not in written]
+    assert torch.equal(pool[keep], before[keep])

@@ -256,3 +256,15 @@ def test_auto_planner_splits_few_heads_only():
     assert kda.prefill_workspace_size(1, 96, 8192) == 0
     assert kda.prefill_workspace_size(64, 96, 540672) == 0
     assert kda.prefill_workspace_size(1, 8, 1 << 20) > 0
+
+
+@pytest.mark.parametrize("H,lens", [(1, [9000]), (130, [129, 64]), (7, [300, 1, 700])])
+def test_head_counts(H, lens):
+    """One head (the planner then splits the 9000-token sequence in two), more heads than
+    SMs (130: a grid wider than the GPU), and an odd count with packed sequences and
+    checkpoints.  Every unit against the oracle for the small cases, sampled heads for 130."""
+    inp = inputs.make_prefill(lens, H=H, seed=300 + H, device="cpu", s0_std=0.02, ckpt_every=64)
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    units = None if H < 100 else [(s, h) for s in range(len(lens)) for h in (0, 1, 64, 127, 129)]
+    check_against_oracle(inp, o, S, ck, units=units)
