@@ -27,6 +27,7 @@ namespace kda {
 namespace {
 
 constexpr int kMaxHostBlocks = 64;
+constexpr int64_t kTailTokens = 256;  // size of the last block when the final stretch allows
 
 struct HostBlock {
   int64_t a, e;  // token rows [a, e)
@@ -49,14 +50,17 @@ __global__ void block_cu_kernel(const int32_t* __restrict__ cu, const BlockTable
   }
 }
 
-// Block borders: about `target` tokens each; a border that falls inside a sequence moves
-// down to that sequence's chunk grid (a multiple of 64 tokens from its start), or up when
-// that would leave the block empty.
+// Block borders: about `target` tokens each, the last one about kTailTokens; a border
+// that falls inside a sequence moves down to that sequence's chunk grid (a multiple of 64
+// tokens from its start), or up when that would leave the block empty.
 bool plan_borders(const int32_t* cu, int n_seq, int64_t T, int64_t target, std::vector<int64_t>& border) {
   border.assign(1, 0);
   int k = 0;
   for (int64_t a = 0; a < T;) {
-    int64_t e = std::min(a + target, T);
+    // the last block's compute and download are the part no upload overlaps: a final stretch
+    // longer than 2 kTailTokens ends with a block of about kTailTokens
+    const int64_t left = T - a;
+    int64_t e = (left <= target && left > 2 * kTailTokens) ? T - kTailTokens : std::min(a + target, T);
     while (k < n_seq && cu[k + 1] <= e) ++k;  // first sequence ending after e: the one e may cut
     if (e < T && k < n_seq && cu[k] < e) {
       const int64_t base = cu[k];

@@ -54,8 +54,12 @@ def test_hand_example():
 
 
 def test_single_sequence_default():
-    assert check_borders([8192], 0) == list(range(0, 8193, 1024))
+    """1024-token blocks; the final stretch (1024 tokens) ends with a 256-token block, the
+    part of the pipeline no upload overlaps."""
+    assert check_borders([8192], 0) == list(range(0, 8192, 1024)) + [7936, 8192]
     assert check_borders([100], 0) == [0, 100]
+    assert check_borders([600], 0) == [0, 320, 600]  # tail split at 344, moved down to the chunk grid
+    assert check_borders([500], 0) == [0, 500]        # at most 2 x 256 tokens: one block
 
 
 @pytest.mark.parametrize("seed", range(20))
