@@ -13,11 +13,11 @@
 // Decay range.  K_inv = K / a is not representable over 64 tokens (with g >= -5 the
 // cumulative log-decay reaches -320).  The pages bound the log-decay of a 16-token tile
 // by -80 ("Kimi K3.1 Pro 架构完全拆解" 3.2), so the products for L and M_qk are formed
-// per 16-token row block tb with reference token b = 16 tb:
-//     row side    QA[t] = Q[t] exp(G[t] - G[b_tb(t)])              (<= 1)
-//     column side B_tb[s] = K[s] exp(G[b_tb] - G[s]),  s < 16 (tb + 1)
-//                 = K[s] exp(G[b_sb(s)] - G[s]) * exp(G[b_tb] - G[b_sb(s)])
-//                   (first factor in [1, e^75], second <= 1)
+// per 16-token row block tb with the reference Gx[tb], the cumulative log-decay just
+// before the block (Gx[0] = 0):
+//     row side    QA[t] = Q[t] exp(G[t] - Gx[tb(t)])                (<= 1)
+//     column side B_tb[s] = K[s] exp(Gx[tb] - G[s]),  s < 16 (tb + 1)
+//                   (<= e^80 for s in block tb, the pages' 16-token bound; <= 1 before it)
 // and row block tb reads its entries from the product with B_tb.  The four B_tb are
 // stacked into one 160-row operand, so one dense bf16 GEMM (M = 128, N = 160) forms
 // every tile, the diagonal ones included; nothing overflows.
