@@ -135,3 +135,15 @@ def test_verify_workload_sampled():
     assert rel_max(host(o[bsel]), ref["o"]) <= DECODE_TOL
     assert rel_max(host(S[bsel]), ref["S"]) <= DECODE_TOL
     assert np.array_equal(host(cache[bsel]), ref["conv_cache"])
+
+
+@pytest.mark.parametrize("z_val,b_val", [(30.0, 30.0), (-30.0, -30.0), (30.0, -30.0)])
+def test_saturated_gates(z_val, b_val):
+    """z = +-30 puts the decay at g_min or 0 (alpha = e^-5 or 1), b = +-30 puts beta at 1 or
+    0: the gates' saturated ends, against the oracle."""
+    x = inputs.make_decode_frontend(3, 4, 2, W=3, seed=54, commit="random")
+    x.z.fill_(z_val)
+    x.b.fill_(b_val)
+    o, S, cache, st = run(x, "silu")
+    assert st == 0
+    check(x, o, S, cache, reference(x, "silu"))

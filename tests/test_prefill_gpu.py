@@ -268,3 +268,20 @@ def test_head_counts(H, lens):
     assert st == 0
     units = None if H < 100 else [(s, h) for s in range(len(lens)) for h in (0, 1, 64, 127, 129)]
     check_against_oracle(inp, o, S, ck, units=units)
+
+
+@pytest.mark.parametrize("case", ["beta0", "beta1", "g0"])
+def test_degenerate_gates(case):
+    """beta = 0 (the state only decays: o_t = (e^{G_t} S0)^T q_t), beta = 1 (full delta-rule
+    overwrite) and g = 0 (no decay at all, the rebasing's trivial case), packed, with
+    checkpoints, against the oracle."""
+    inp = inputs.make_prefill([200, 64, 130], H=2, seed=400, device="cpu", s0_std=0.02, ckpt_every=64)
+    if case == "beta0":
+        inp.beta.zero_()
+    elif case == "beta1":
+        inp.beta.fill_(1.0)
+    else:
+        inp.g.zero_()
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck)
