@@ -341,6 +341,47 @@ def pin_epilogue_eps_closed_form():
 ALL_PINS += [pin_epilogue_hand_values, pin_epilogue_invariants, pin_epilogue_eps_closed_form]
 
 
+def pin_value_rotation():
+    """The recurrence acts on the value side (d_v) by right multiplication only
+    ([p1] 3.1: S_t = (I - beta k k^T) Diag(alpha) S_{t-1} + beta k v^T): for any orthogonal R,
+    v -> v R and S0 -> S0 R give o -> o R and S -> S R.  A transposed state or read-out, or a
+    decay applied on the value side, breaks it."""
+    T, H, d = 37, 2, 16
+    c = rand_case(T, H, d, seed=41)
+    rng = np.random.default_rng(42)
+    R, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    base = run(c)
+    c2 = dict(c)
+    c2["v"] = (c["v"].astype(np.float64) @ R).astype(np.float32)
+    c2["S0"] = (c["S0"].astype(np.float64) @ R).astype(np.float32)
+    rot = run(c2)
+    want_o = base["o"] @ R
+    want_S = base["S_out"] @ R
+    scale = np.abs(want_o).max()
+    assert np.abs(rot["o"] - want_o).max() <= 1e-5 * scale, np.abs(rot["o"] - want_o).max()
+    assert np.abs(rot["S_out"] - want_S).max() <= 1e-5 * np.abs(want_S).max()
+
+
+def pin_key_permutation():
+    """The decay is diagonal in d_k ([p1] 3.1-3.2): permuting the key channels of q, k, g
+    and the rows of S0 together leaves o unchanged and permutes the rows of S.  A decay
+    applied on the wrong axis or a mixed-up channel index breaks it."""
+    T, H, d = 29, 2, 16
+    c = rand_case(T, H, d, seed=43, decay="uniform")
+    perm = np.random.default_rng(44).permutation(d)
+    base = run(c)
+    c2 = dict(c)
+    for key in ("q", "k", "g"):
+        c2[key] = np.ascontiguousarray(c[key][..., perm])
+    c2["S0"] = np.ascontiguousarray(c["S0"][:, :, perm, :])
+    pm = run(c2)
+    assert np.allclose(pm["o"], base["o"], rtol=1e-12, atol=1e-14)
+    assert np.allclose(pm["S_out"], base["S_out"][:, :, perm, :], rtol=1e-12, atol=1e-14)
+
+
+ALL_PINS += [pin_value_rotation, pin_key_permutation]
+
+
 # --------------------------------------------------------------------- decode front end
 # oracle/frontend.py: "Kimi K3 的架構 ... 服務性能" section 7 (short causal convolution, q/k L2
 # normalisation, alpha and beta gates) and "Kimi K3.1 Pro 架构完全拆解" 3.2 (bounded decay
