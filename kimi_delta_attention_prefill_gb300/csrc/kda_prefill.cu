@@ -28,8 +28,10 @@
 // on the CUDA cores.  The state lives in TMEM in fp32 for the whole sequence.
 //
 // Execution.  One CTA of 384 threads per work item, in two warp groups:
-//   recurrent (warps 0-3): the serial chain of chunk n -- K_decay S and Q_decay S, X,
-//       U, the state update and O -- on tcgen05 with the state resident in TMEM;
+//   recurrent (warps 0-3): the serial chain of chunk n -- X = V - K_decay S and
+//       Q_decay S (one product: the prep writes -K_decay, and V enters the accumulator
+//       through an identity operand held in TMEM), U, the state update and O -- on
+//       tcgen05 with the state resident in TMEM;
 //   prep (warps 4-11): everything that does not depend on the state, for chunk n + 1 --
 //       loads, cumsum, decay factors, scaled operands, L / M_qk, INV -- so it overlaps
 //       the recurrence ("部署 Kimi K3 ..." 1.1: overlap the intra-chunk work with the
@@ -64,15 +66,17 @@ constexpr int kTotCg = 12, kTotPitch = 16 * kTotCg;
 
 // TMEM columns (all 128-lane layouts: lane = row of D).
 //   TS  [0, 128)   the state S, fp32 (lane = d_k row)
-//   TR1 [128, 256) lanes 0-63: P = K_decay S, then U; lanes 64-127: Q_decay S, then O
+//   TR1 [128, 256) lanes 0-63: X = V - K_decay S, then U; lanes 64-127: Q_decay S, then O
 //   TLM [256, 416) lanes 0-63: M_qk rows, lanes 64-127: L rows, 160 columns (4 blocks)
 //   TF  [416, 480) lanes 64-127: output-stage factors sigmoid(a) w, packed half2 (recurrent)
-constexpr uint32_t kTS = 0, kTR1 = 128, kTLM = 256, kTF = 416;
+//   TI  [480, 512) [I_64; 0] as bf16 pairs (lane = row, column = two K entries): the A
+//                  operand of the product that adds V to rows 0-63 of TR1
+constexpr uint32_t kTS = 0, kTR1 = 128, kTLM = 256, kTF = 416, kTI = 480;
 __host__ __device__ constexpr uint32_t lm_col(int tb) { return tb == 0 ? 0u : tb == 1 ? 16u : tb == 2 ? 48u : 96u; }
 
 // Shared memory (bytes from a 1024-aligned base).
 constexpr uint32_t SM_S16 = 0;        // S fp16, [i][j], 2 N-panels x 128 rows        (recurrent)
-constexpr uint32_t SM_KQ = 32768;     // [K_decay; Q_decay] fp16, K-major, 2 x 128 rows (prep -> recurrent)
+constexpr uint32_t SM_KQ = 32768;     // [-K_decay; Q_decay] fp16, K-major, 2 x 128 rows (prep -> recurrent)
 constexpr uint32_t SM_V = 65536;      // v tiles (TMA), two stages of 16 KiB             (recurrent)
 constexpr uint32_t SM_XU = 98304;     // X, then U, fp16 [t][j], 2 N-panels x 64 rows    (recurrent)
 constexpr uint32_t SM_KR = 114688;    // K_restore fp16 [t][i], 2 M-panels x 64 rows     (prep -> recurrent)
@@ -88,7 +92,8 @@ constexpr uint32_t SM_AL = SM_TOT + 7168;      // fp32 [2][128] a_last by chunk 
 constexpr uint32_t SM_BETA = SM_AL + 1024;     // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;     // mbarriers
 constexpr uint32_t SM_CTRL = SM_BAR + 128;     // tmem base, flags
-constexpr uint32_t kSmemBytes = SM_CTRL + 64;
+constexpr uint32_t SM_W = SM_CTRL + 64;      // output-stage weight w as 64 half2 (recurrent)
+constexpr uint32_t kSmemBytes = SM_W + 256;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 static_assert(SM_BT + 40960 == SM_MISC, "layout");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -96,7 +101,7 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 enum {
   BAR_V0 = 0, BAR_V1 = 1,  // v tile landed (TMA)
   BAR_LM = 2,              // L / M_qk product done (prep's MMA)
-  BAR_M1 = 3,              // K_decay S, Q_decay S done
+  BAR_M1 = 3,              // X = V - K_decay S, Q_decay S done
   BAR_M2 = 4,              // U done
   BAR_M34 = 5,             // state update and O done
   BAR_KQ = 6,              // prep -> recurrent: [K_decay; Q_decay] of the chunk written
@@ -393,8 +398,8 @@ template <bool kHook>
 __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                            uint32_t tmem, int n_chunks, int ptid) {
   // Registers: the launch gives every thread 168; the recurrent group gives some back
-  // (128 x 104) so the prep group can hold its operand tiles (256 x 192); 62,464 of the
-  // block's 64,512 registers in total.
+  // (128 x 120) so the prep group can hold its operand tiles (256 x 192): all 64,512 of
+  // the block's registers.
   asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
   const int pw = ptid >> 5, lane = ptid & 31;
   const int tb = pw >> 1, tql = lane >> 3;
@@ -564,7 +569,8 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     }
 
     // ---- 3. scaled operands.  Raw q, k (loaded above) are replaced in place in the
-    //         [K_decay; Q_decay] buffer (the recurrence released it before the copy).
+    //         [K_decay; Q_decay] buffer (the recurrence released it before the copy);
+    //         K_decay is stored negated, so the recurrence's product gives -K_decay S.
     const int valid = min(kChunk, w.len - cidx * kChunk);
     uint32_t krq[4][4];
     {
@@ -593,7 +599,7 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           qd2[e] = pack_half2(qa[2 * e] * atr[2 * e], qa[2 * e + 1] * atr[2 * e + 1]);
-          kd2[e] = pack_half2(ka[2 * e] * atr[2 * e], ka[2 * e + 1] * atr[2 * e + 1]);
+          kd2[e] = pack_half2(-(ka[2 * e] * atr[2 * e]), -(ka[2 * e + 1] * atr[2 * e + 1]));
           krq[u][e] = pack_half2(kb[2 * e] * rtr[2 * e], kb[2 * e + 1] * rtr[2 * e + 1]);
           qa2[e] = pack_bf162(qa[2 * e], qa[2 * e + 1]);
           ka2[e] = pack_bf162(ka[2 * e], ka[2 * e + 1]);
@@ -739,7 +745,7 @@ __device__ __forceinline__ void sigmoid_w_half2(const uint4& a8, const uint32_t 
 template <bool kHook>
 __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                                 uint32_t tmem, int n_chunks, bool do_o, bool v_zero, bool entry_identity, int tid) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory");
   const int rw = tid >> 5;
   const uint32_t tl = static_cast<uint32_t>(rw * 32) << 16;
   const uint64_t dS16 = smem_desc(smem_u32(sm + SM_S16), 16384, 1024, kSwizzle128B);
@@ -749,6 +755,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   const uint64_t dIM = smem_desc(smem_u32(sm + SM_IM), 16, 1024, kSwizzle128B);
   const uint32_t id_k_mn = idesc_f16(128, 128, false, false, true);
   const uint32_t id_mn_mn = idesc_f16(128, 128, false, true, true);
+  const uint32_t id_v = idesc_f16(128, 128, true, false, true);
   const float* alast = reinterpret_cast<const float*>(sm + SM_AL);
   const int i = tid;  // state row owned by this thread
   const bool gated = p.gate != nullptr && do_o;  // output stage on the o rows
@@ -779,6 +786,13 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     for (int e = 0; e < 32; ++e) r[e] *= al0;
     tmem_st32(tmem + tl + kTS + c0, r);
   }
+  {  // [I_64; 0] (bf16 pairs) in TMEM: the A operand that adds V to rows 0-63 of P's accumulator
+    float r[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      r[e] = __uint_as_float((i < 64 && e == (i >> 1)) ? ((i & 1) ? 0x3F800000u : 0x00003F80u) : 0u);
+    tmem_st32(tmem + tl + kTI, r);
+  }
   tmem_wait_st();
   if (tid == 0) {
     for (int s = 0; s < 2 && s < n_chunks; ++s) {
@@ -787,6 +801,10 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       tma_load_3d(sm + SM_V + s * 16384, &p.tm_v, &bars[BAR_V0 + s], 0, w.h, r0);
       tma_load_3d(sm + SM_V + s * 16384 + 8192, &p.tm_v, &bars[BAR_V0 + s], 64, w.h, r0);
     }
+  }
+  if (gated && tid < 64) {
+    const float w0 = p.norm_weight ? p.norm_weight[2 * tid] : 1.f, w1 = p.norm_weight ? p.norm_weight[2 * tid + 1] : 1.f;
+    reinterpret_cast<uint32_t*>(sm + SM_W)[tid] = pack_half2(w0, w1);
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -813,7 +831,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       tma_load_3d(sm + SM_V + (vs ^ 1) * 16384 + 8192, &p.tm_v, &bars[BAR_V0 + (vs ^ 1)], 64, w.h, r0);
     }
 
-    // ---- P = K_decay S, Q_decay S (one M = 128 product)
+    // ---- [X; Q_decay S] = [-K_decay; Q_decay] S + [I_64; 0] V (one M = 128 accumulator)
     if (!kwait<kHook>(&bars[BAR_KQ], n & 1)) ctrl[CTRL_ABORT] = 1;
     if (tid == 0) {
       tc_fence_after();
@@ -821,34 +839,38 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       for (int kk = 0; kk < 8; ++kk)
         mma_f16(tmem + kTR1, dKQ + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4), dS16 + ((kk * 2048) >> 4), id_k_mn,
                 kk > 0);
+      // V enters rows 0-63 through the identity operand in TMEM (bf16, like the v tile)
+      if (!kwait<kHook>(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
+      tc_fence_after();
+      if (!v_zero) {
+        const uint64_t dV = smem_desc(smem_u32(sm + SM_V + vs * 16384), 8192, 1024, kSwizzle128B);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_f16_ta(tmem + kTR1, tmem + kTI + 8 * kk, dV + ((kk * 2048) >> 4), id_v, 1);
+      }
       mma_commit(&bars[BAR_M1]);
     }
-    // ---- X = V - P (rows past the sequence end are zero)
-    //      Warps 0-1 own rows 0-63 (P, X, U); warps 2-3 meanwhile prepare the output stage.
+    // ---- X -> fp16 operand (rows past the sequence end are zero)
+    //      Warps 0-1 own rows 0-63 (X, U); warps 2-3 meanwhile prepare the output stage.
     if (rw < 2) {
-      if (!kwait<kHook>(&bars[BAR_M1], n & 1) || !kwait<kHook>(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
+      if (!kwait<kHook>(&bars[BAR_M1], n & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
       if (tid == 0 && n + 1 < n_chunks) issue_qk(p, w, sm, bars, cidx + 1);  // the buffer is free again
       {
         const int t = tid;
         const bool mk = t < valid;
-        const uint8_t* vt = sm + SM_V + vs * 16384;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           float r[32];
           tmem_ld32(tmem + tl + kTR1 + g * 32, r);
-          const uint8_t* vp = vt + (g >> 1) * 8192;
           uint8_t* xp = sm + SM_XU + (g >> 1) * 8192;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            float vv[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(vp + sw128(t, 64 * (g & 1) + 16 * c)), vv);
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = mk ? (v_zero ? 0.f : vv[e]) - r[8 * c + e] : 0.f;
-            st4(xp + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]),
-                pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+            const float* x = r + 8 * c;
+            st4(xp + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(mk ? x[0] : 0.f, mk ? x[1] : 0.f),
+                pack_half2(mk ? x[2] : 0.f, mk ? x[3] : 0.f), pack_half2(mk ? x[4] : 0.f, mk ? x[5] : 0.f),
+                pack_half2(mk ? x[6] : 0.f, mk ? x[7] : 0.f));
           }
+          asm volatile("" ::: "memory");  // one 32-column group live at a time
         }
       }
       fence_proxy_async_smem();
@@ -906,21 +928,27 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       const int t = tid - 64;
       const bool wr = t < valid;
       const uint4* arow = reinterpret_cast<const uint4*>(p.gate + ((row0 + t) * p.H + w.h) * kHeadDim);
+      const uint4* wsm = reinterpret_cast<const uint4*>(sm + SM_W);
+      // logits of the next 32 columns are in flight while these 32 are converted
+      uint4 nx[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) nx[c] = wr ? __ldg(arow + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 cur[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cur[c] = nx[c];
+        if (q4 < 3) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) nx[c] = wr ? __ldg(arow + 4 * (q4 + 1) + c) : make_uint4(0, 0, 0, 0);
+        }
         float f[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t w2[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};  // ones
-          if (p.norm_weight) {
-            const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.norm_weight + 32 * q4 + 8 * c));
-            const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.norm_weight + 32 * q4 + 8 * c + 4));
-            w2[0] = pack_half2(w0.x, w0.y); w2[1] = pack_half2(w0.z, w0.w);
-            w2[2] = pack_half2(w1.x, w1.y); w2[3] = pack_half2(w1.z, w1.w);
-          }
-          const uint4 a8 = wr ? __ldg(arow + 4 * q4 + c) : make_uint4(0, 0, 0, 0);
+          const uint4 wv = wsm[4 * q4 + c];
+          const uint32_t w2[4] = {wv.x, wv.y, wv.z, wv.w};
           uint32_t fc[4];
-          sigmoid_w_half2(a8, w2, fc);
+          sigmoid_w_half2(cur[c], w2, fc);
 #pragma unroll
           for (int e = 0; e < 4; ++e) f[4 * c + e] = __uint_as_float(fc[e]);
         }
@@ -967,22 +995,26 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       const float scale = rsqrtf(ss * (1.f / kHeadDim) + p.eps);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float r[32], f[16];
-        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+        float f[16];
         tmem_ld16(tmem + tl + kTF + g * 16, f);
-        if (wr) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + g * 32);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float y[8];
+        for (int h = 0; h < 2; ++h) {  // 16 columns at a time: the factors and one half live
+          float r[16];
+          tmem_ld16(tmem + tl + kTR1 + g * 32 + 16 * h, r);
+          if (wr) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + g * 32 + 16 * h);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&f[4 * c + e]));
-              y[2 * e] = r[8 * c + 2 * e] * scale * ff.x;
-              y[2 * e + 1] = r[8 * c + 2 * e + 1] * scale * ff.y;
+            for (int c = 0; c < 2; ++c) {
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&f[8 * h + 4 * c + e]));
+                y[2 * e] = r[8 * c + 2 * e] * scale * ff.x;
+                y[2 * e + 1] = r[8 * c + 2 * e + 1] * scale * ff.y;
+              }
+              dst[c] = make_uint4(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]), pack_bf162(y[4], y[5]),
+                                  pack_bf162(y[6], y[7]));
             }
-            dst[c] = make_uint4(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]), pack_bf162(y[4], y[5]),
-                                pack_bf162(y[6], y[7]));
           }
         }
       }
