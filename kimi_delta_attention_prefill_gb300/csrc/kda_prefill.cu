@@ -57,7 +57,8 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kRThreads = 128;  // recurrent group: warps 0-3 (TMEM lane quarters 0-3)
 constexpr int kPThreads = 256;  // prep group: warps 4-11
-constexpr uint32_t kBarR = 1, kBarP = 2, kBarXU = 3;  // named barrier ids (kBarXU: recurrent warps 0-1)
+constexpr uint32_t kBarR = 1, kBarP = 2, kBarXU = 3, kBarL = 4;  // named barrier ids (kBarXU: recurrent
+                                                              // warps 0-1; kBarL: the prep warps that read L)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Block totals table: [4 blocks][16 channel groups], 12 floats per group (8 used), so the
@@ -289,9 +290,11 @@ __device__ void invert_unit_lower(const float* WL, float* WI, float* PT, int pti
   auto P = [&](int k) { return PT + 320 * k; };  // 16 x 16 blocks, row stride kLdp
 
   // D_b = (I + L_bb)^-1: thread (b, c) forms column c by forward substitution, pushing
-  // each finished x[m] into the rows below it (a 15-step dependency chain).
-  if (ptid < 64) {
-    const int b = ptid >> 4, c = ptid & 15;
+  // each finished x[m] into the rows below it (a 15-step dependency chain).  Threads
+  // 64-127 (prep warps 2-3) read L out of TMEM themselves, so they start as soon as the
+  // other L readers are done (kBarL), while the M_qk readers may still be storing.
+  if (ptid >= 64 && ptid < 128) {
+    const int b = (ptid - 64) >> 4, c = ptid & 15;
     const float* Lb = L(b, b);
     float x[16];
 #pragma unroll
@@ -637,10 +640,11 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     if (!kwait<kHook>(&bars[BAR_LM], n & 1)) ctrl[CTRL_ABORT] = 1;
     tc_fence_after();
     if (ptid == 0 && has_next) issue_g(cidx + 1);  // QA / KA consumed: the region takes the next g
-    if (n > 0 && !kwait<kHook>(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
     {
       const int q = pw & 3, part = pw >> 2;  // TMEM lane quarter; two warps split its columns
       const bool is_l = q >= 2;
+      // only M_qk's rows of [INV Diag(beta); M_qk] are read by the previous chunk's O product
+      if (!is_l && n > 0 && !kwait<kHook>(&bars[BAR_M34], (n - 1) & 1)) ctrl[CTRL_ABORT] = 1;
       const int t = (q & 1) * 32 + lane;
       const int tbl = t >> 4;
       const int g0 = (q & 1) ? 3 : 0, ng = (q & 1) ? 7 : 3, nh = (ng + 1) >> 1;
@@ -684,13 +688,16 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         }
       }
     }
-    named_bar_sync(kBarP, kPThreads);
+    // the L readers (warps 2, 3, 6, 7) meet before the diagonal blocks are inverted; the
+    // M_qk readers join at INV's first group-wide barrier
+    if ((pw & 3) >= 2) named_bar_sync(kBarL, 128);
 
     // ---- 5. INV = (I + L)^-1
     invert_unit_lower(reinterpret_cast<const float*>(sm + SM_WL), reinterpret_cast<float*>(sm + SM_WI),
                       reinterpret_cast<float*>(sm + SM_PT), ptid);
 
-    // ---- 6. INV Diag(beta) and K_restore (their buffers were released before step 4)
+    // ---- 6. INV Diag(beta) and K_restore (their buffers are free: the M_qk readers waited for
+    //         the previous chunk's update before INV's first group-wide barrier)
     put_inv_beta(reinterpret_cast<const float*>(sm + SM_WI), s_beta, sm + SM_IM, ptid);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
