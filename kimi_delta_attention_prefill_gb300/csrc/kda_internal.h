@@ -100,17 +100,27 @@ struct PrefillArgs {
 // rank holds few heads).  A function of the sequence's own length, H, the SM count and
 // the caller's request only, so a sequence is split the same way packed or alone.
 //   n_segments > 0 : min(n_segments, chunks)
-//   n_segments = 0 : min(num_sms / H, chunks / kMinSegChunks), at least 1
+//   n_segments = 0 : the count with the least chain time in a wave model: with n segments
+//     pass 1 runs H (2n - 3) work items and pass 3 H (n - 1), each 1/n of the sequence's
+//     chain, so the time is (ceil(H (2n - 3) / S) + ceil(H (n - 1) / S)) / n of the
+//     unsplit chain (S = SMs, one CTA each); n = 1 costs 1 and ties keep the smaller n.
+//     Candidates: n <= S / H + 1 and n <= chunks / kMinSegChunks.
 constexpr int kMinSegChunks = 64;  // segments shorter than 4096 tokens do not pay for the extra passes
 
 __host__ __device__ inline int plan_segments(int len, int H, int num_sms, int n_segments) {
   const int nch = (len + kChunk - 1) / kChunk;
   if (nch <= 1) return 1;
   if (n_segments > 0) return n_segments < nch ? n_segments : nch;
-  const int target = num_sms / (H > 0 ? H : 1);
-  const int by_len = nch / kMinSegChunks;
-  const int n = target < by_len ? target : by_len;
-  return n < 1 ? 1 : n;
+  const int h = H > 0 ? H : 1, S = num_sms > 0 ? num_sms : 1;
+  int nmax = S / h + 1;
+  if (nch / kMinSegChunks < nmax) nmax = nch / kMinSegChunks;
+  int best = 1;
+  int64_t best_w = 1, best_n = 1;  // cost best_w / best_n, compared as cross products
+  for (int n = 2; n <= nmax; ++n) {
+    const int64_t w = (static_cast<int64_t>(h) * (2 * n - 3) + S - 1) / S + (static_cast<int64_t>(h) * (n - 1) + S - 1) / S;
+    if (w * best_n < best_w * n) { best = n; best_w = w; best_n = n; }
+  }
+  return best;
 }
 
 // Work-item modes of the prefill kernel.
@@ -142,9 +152,11 @@ __host__ inline SplitLayout split_layout(int n_seq, int H, int64_t total_tokens,
     const int64_t b = total_tokens / kChunk + n_seq;
     extra = a < b ? a : b;
   } else if (n_segments == 0) {
-    const int target = num_sms / (H > 0 ? H : 1);
-    if (target >= 2) {
-      const int64_t a = static_cast<int64_t>(n_seq) * (target - 1);
+    // the planner's count only grows with the length: a sequence of all the tokens bounds it
+    const int most = plan_segments(total_tokens < (int64_t{1} << 30) ? static_cast<int>(total_tokens) : (1 << 30), H,
+                                   num_sms, 0);
+    if (most >= 2) {
+      const int64_t a = static_cast<int64_t>(n_seq) * (most - 1);
       const int64_t b = total_tokens / (static_cast<int64_t>(kChunk) * kMinSegChunks);
       extra = a < b ? a : b;
     }

@@ -140,6 +140,32 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         kda.library()
 
 
+def _split_bytes(n_seq, H, extra):
+    """The split workspace for `extra` extra segments (layout in kda_internal.h: counts,
+    two item tables, per-sequence info, then [slots][H][3][128][128] fp32)."""
+    up = lambda x: (x + 255) // 256 * 256
+    max1, max3 = n_seq + 2 * extra, extra
+    n_slots = min(2 * extra, n_seq + extra)
+    off3 = up(256 + 16 * max1)
+    offs = up(off3 + 16 * max3)
+    offsl = up(offs + 8 * n_seq)
+    return offsl + n_slots * H * 3 * 128 * 128 * 4
+
+
+def test_planner_wave_model(lib):
+    """The automatic segment count minimises (ceil(H(2n-3)/S) + ceil(H(n-1)/S)) / n with
+    S = 152 (the library's assumption without a GPU); worked by hand:
+    H = 8, 2^20 tokens: n = 20 (pass 1: 296 items = 2 waves, pass 3: 152 = 1 wave, 3/20);
+    n = 19 would give 3/19 and n = 21 5/21.  H = 16: n = 10 (272 and 144 items, 3/10; 9 gives
+    3/9).  One head, 9000 tokens: at most 2 segments by length, and 2 segments cost 2/2 = 1,
+    a tie with no split, which the planner keeps."""
+    assert kda.prefill_workspace_size(1, 8, 1 << 20) == _split_bytes(1, 8, 19)
+    assert kda.prefill_workspace_size(1, 16, 1 << 20) == _split_bytes(1, 16, 9)
+    assert kda.prefill_workspace_size(1, 1, 9000) == 0
+    # a forced count is taken as given (bounded by the chunks)
+    assert kda.prefill_workspace_size(1, 8, 1 << 20, n_segments=19) == _split_bytes(1, 8, 18)
+
+
 def test_workspace_sizes(lib):
     # without a GPU the library assumes 152 SMs for the planner's bound
     assert kda.prefill_workspace_size(1, 96, 8192) == 0

@@ -260,7 +260,8 @@ def test_auto_planner_splits_few_heads_only():
 
 @pytest.mark.parametrize("H,lens", [(1, [9000]), (130, [129, 64]), (7, [300, 1, 700])])
 def test_head_counts(H, lens):
-    """One head (the planner then splits the 9000-token sequence in two), more heads than
+    """One head (a 9000-token sequence: two segments would not shorten the chain, so the
+    planner keeps one), more heads than
     SMs (130: a grid wider than the GPU), and an odd count with packed sequences and
     checkpoints.  Every unit against the oracle for the small cases, sampled heads for 130."""
     inp = inputs.make_prefill(lens, H=H, seed=300 + H, device="cpu", s0_std=0.02, ckpt_every=64)
