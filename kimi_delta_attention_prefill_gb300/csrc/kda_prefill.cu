@@ -575,6 +575,15 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     //         [K_decay; Q_decay] buffer (the recurrence released it before the copy);
     //         K_decay is stored negated, so the recurrence's product gives -K_decay S.
     const int valid = min(kChunk, w.len - cidx * kChunk);
+    uint64_t atr2[4], natr2[4], rtr2[4], fr2[3][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      atr2[e] = f32x2(atr[2 * e], atr[2 * e + 1]);
+      natr2[e] = f32x2(-atr[2 * e], -atr[2 * e + 1]);
+      rtr2[e] = f32x2(rtr[2 * e], rtr[2 * e + 1]);
+#pragma unroll
+      for (int j = 0; j < 3; ++j) fr2[j][e] = f32x2(fr[j][2 * e], fr[j][2 * e + 1]);
+    }
     uint32_t krq[4][4];
     {
       uint8_t* kqp = sm + SM_KQ + kpanel * 16384;
@@ -588,38 +597,40 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         bf16x8_to_f32(rq[u], qf);
         bf16x8_to_f32(rk[u], kf);
         const bool m = t < valid;
-        float qa[8], ka[8], kb[8];
-        uint32_t qd2[4], kd2[4], qa2[4], ka2[4];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float kk = m ? kf[e] : 0.f;
-          const float E = exp2_fast(G[u][e]);    // in [e^-80, 1]
-          const float Ei = exp2_fast(-G[u][e]);  // in [1, e^80]
-          qa[e] = qf[e] * E;
-          ka[e] = kk * E;
-          kb[e] = kk * Ei;
-        }
+        // channel pairs (2p, 2p + 1) in packed two-lane multiplies
+        uint64_t qa[4], ka[4], kb[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          qd2[e] = pack_half2(qa[2 * e] * atr[2 * e], qa[2 * e + 1] * atr[2 * e + 1]);
-          kd2[e] = pack_half2(-(ka[2 * e] * atr[2 * e]), -(ka[2 * e + 1] * atr[2 * e + 1]));
-          krq[u][e] = pack_half2(kb[2 * e] * rtr[2 * e], kb[2 * e + 1] * rtr[2 * e + 1]);
-          qa2[e] = pack_bf162(qa[2 * e], qa[2 * e + 1]);
-          ka2[e] = pack_bf162(ka[2 * e], ka[2 * e + 1]);
+          const float E0 = exp2_fast(G[u][2 * e]), E1 = exp2_fast(G[u][2 * e + 1]);      // in [e^-80, 1]
+          const float I0 = exp2_fast(-G[u][2 * e]), I1 = exp2_fast(-G[u][2 * e + 1]);  // in [1, e^80]
+          const uint64_t kk = f32x2(m ? kf[2 * e] : 0.f, m ? kf[2 * e + 1] : 0.f);
+          const uint64_t E = f32x2(E0, E1);
+          qa[e] = mul_f32x2(f32x2(qf[2 * e], qf[2 * e + 1]), E);
+          ka[e] = mul_f32x2(kk, E);
+          kb[e] = mul_f32x2(kk, f32x2(I0, I1));
+        }
+        uint32_t qd2[4], kd2[4], qa2[4], ka2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qd2[e] = half2_of(mul_f32x2(qa[e], atr2[e]));
+          kd2[e] = half2_of(mul_f32x2(ka[e], natr2[e]));
+          krq[u][e] = half2_of(mul_f32x2(kb[e], rtr2[e]));
+          qa2[e] = bf162_of(qa[e]);
+          ka2[e] = bf162_of(ka[e]);
         }
         st4(kqp + sk, kd2[0], kd2[1], kd2[2], kd2[3]);
         st4(kqp + sq, qd2[0], qd2[1], qd2[2], qd2[3]);
         st4(qap + sk, qa2[0], qa2[1], qa2[2], qa2[3]);
         st4(qap + sq, ka2[0], ka2[1], ka2[2], ka2[3]);  // KA rows 64..127 share q's swizzle phase
         // column-side operands: this block's rows of B_tb2 for every row block tb2 >= tb
-        st4(btp + sw128(lm_col(tb) + t, 16 * kchunk), pack_bf162(kb[0], kb[1]), pack_bf162(kb[2], kb[3]),
-            pack_bf162(kb[4], kb[5]), pack_bf162(kb[6], kb[7]));
+        st4(btp + sw128(lm_col(tb) + t, 16 * kchunk), bf162_of(kb[0]), bf162_of(kb[1]), bf162_of(kb[2]),
+            bf162_of(kb[3]));
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
           if (tb + 1 + j > 3) break;
-          st4(btp + sw128(lm_col(tb + 1 + j) + t, 16 * kchunk),
-              pack_bf162(kb[0] * fr[j][0], kb[1] * fr[j][1]), pack_bf162(kb[2] * fr[j][2], kb[3] * fr[j][3]),
-              pack_bf162(kb[4] * fr[j][4], kb[5] * fr[j][5]), pack_bf162(kb[6] * fr[j][6], kb[7] * fr[j][7]));
+          st4(btp + sw128(lm_col(tb + 1 + j) + t, 16 * kchunk), bf162_of(mul_f32x2(kb[0], fr2[j][0])),
+              bf162_of(mul_f32x2(kb[1], fr2[j][1])), bf162_of(mul_f32x2(kb[2], fr2[j][2])),
+              bf162_of(mul_f32x2(kb[3], fr2[j][3])));
         }
       }
     }

@@ -279,6 +279,24 @@ __device__ __forceinline__ float exp2_fast(float x) {
   return y;
 }
 
+// Two fp32 values in one 64-bit register (element 0 in the low half) and the packed
+// two-lane fp32 multiply (each lane rounded to nearest, as a scalar multiply).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -286,6 +304,14 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t half2_of(uint64_t a) {
+  const float2 v = unpack_f32x2(a);
+  return pack_half2(v.x, v.y);
+}
+__device__ __forceinline__ uint32_t bf162_of(uint64_t a) {
+  const float2 v = unpack_f32x2(a);
+  return pack_bf162(v.x, v.y);
 }
 
 }  // namespace kda
