@@ -34,6 +34,7 @@
 #include <cstdint>
 
 #include "kda_internal.h"
+#include "kda_ptx.cuh"
 
 namespace kda {
 
@@ -251,16 +252,31 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     __syncthreads();
   }
 
+  // the state as column pairs for packed two-lane fp32 arithmetic (same roundings)
+  uint64_t s2[kRowsPerThread][2];
+#pragma unroll
+  for (int m = 0; m < kRowsPerThread; ++m) {
+    s2[m][0] = f32x2(s[m].x, s[m].y);
+    s2[m][1] = f32x2(s[m].z, s[m].w);
+  }
   for (int i = 0; i < n_tok; ++i) {
     // X = Diag(alpha) S, then partial w = X^T k and p = X^T q over this thread's rows.
-    float4 w = make_float4(0.f, 0.f, 0.f, 0.f), p = w;
+    uint64_t w01 = f32x2(0.f, 0.f), w23 = w01, p01 = w01, p23 = w01;
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) {
       const int row = r0 + 8 * m;
       const float a = sm.alpha[i][row], kk = sm.k[i][row], qq = sm.q[i][row];
-      s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
-      w.x += kk * s[m].x; w.y += kk * s[m].y; w.z += kk * s[m].z; w.w += kk * s[m].w;
-      p.x += qq * s[m].x; p.y += qq * s[m].y; p.z += qq * s[m].z; p.w += qq * s[m].w;
+      const uint64_t a2 = f32x2(a, a), k2 = f32x2(kk, kk), q2 = f32x2(qq, qq);
+      s2[m][0] = mul_f32x2(s2[m][0], a2);
+      s2[m][1] = mul_f32x2(s2[m][1], a2);
+      w01 = fma_f32x2(k2, s2[m][0], w01); w23 = fma_f32x2(k2, s2[m][1], w23);
+      p01 = fma_f32x2(q2, s2[m][0], p01); p23 = fma_f32x2(q2, s2[m][1], p23);
+    }
+    float4 w, p;
+    {
+      const float2 a = unpack_f32x2(w01), b = unpack_f32x2(w23), c = unpack_f32x2(p01), d = unpack_f32x2(p23);
+      w = make_float4(a.x, a.y, b.x, b.y);
+      p = make_float4(c.x, c.y, d.x, d.y);
     }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {  // across the 8 row groups (lane bits 2..4)
@@ -287,14 +303,20 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
         *reinterpret_cast<float4*>(o + ob) = ov;
       }
     }
+    const uint64_t u01 = f32x2(u.x, u.y), u23 = f32x2(u.z, u.w);
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) {
       const float kk = sm.k[i][r0 + 8 * m];
-      s[m].x += kk * u.x; s[m].y += kk * u.y; s[m].z += kk * u.z; s[m].w += kk * u.w;
+      const uint64_t k2 = f32x2(kk, kk);
+      s2[m][0] = fma_f32x2(k2, u01, s2[m][0]);
+      s2[m][1] = fma_f32x2(k2, u23, s2[m][1]);
     }
     if (i + 1 == nc && Sout) {
 #pragma unroll
-      for (int m = 0; m < kRowsPerThread; ++m) __stcs(&Sout[((r0 + 8 * m) * kD + col) >> 2], s[m]);
+      for (int m = 0; m < kRowsPerThread; ++m) {
+        const float2 a = unpack_f32x2(s2[m][0]), b = unpack_f32x2(s2[m][1]);
+        __stcs(&Sout[((r0 + 8 * m) * kD + col) >> 2], make_float4(a.x, a.y, b.x, b.y));
+      }
     }
   }
   if constexpr (kFront) {

@@ -279,8 +279,9 @@ __device__ __forceinline__ float exp2_fast(float x) {
   return y;
 }
 
-// Two fp32 values in one 64-bit register (element 0 in the low half) and the packed
-// two-lane fp32 multiply (each lane rounded to nearest, as a scalar multiply).
+// Two fp32 values in one 64-bit register (element 0 in the low half) and packed two-lane
+// fp32 arithmetic (each lane rounded to nearest, as the scalar instruction; the fma is
+// fused like FFMA).
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -289,6 +290,16 @@ __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
 __device__ __forceinline__ float2 unpack_f32x2(uint64_t a) {
