@@ -44,10 +44,14 @@ constexpr int kD = 128;
 constexpr int kThreads = 256;
 constexpr int kRowsPerThread = 16;
 
+// q, k and alpha are indexed by the state row i (d_k) and kept row-permuted: row i at
+// kp(i) = (i mod 8) x 16 + i / 8, so the 16 rows r, r + 8, ..., r + 120 that a thread
+// owns are 16 consecutive floats (four 16-byte loads).
+__host__ __device__ constexpr int kp(int i) { return (i & 7) * 16 + (i >> 3); }
 struct DecodeSmem {
-  float q[kMaxDecodeTokens][kD];
-  float k[kMaxDecodeTokens][kD];
-  float alpha[kMaxDecodeTokens][kD];
+  alignas(16) float q[kMaxDecodeTokens][kD];
+  alignas(16) float k[kMaxDecodeTokens][kD];
+  alignas(16) float alpha[kMaxDecodeTokens][kD];
   float v[kMaxDecodeTokens][kD];
   float beta[kMaxDecodeTokens];
   float kq[kMaxDecodeTokens];
@@ -113,7 +117,7 @@ __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, in
     const float* wv = fe.conv_w + ((static_cast<int64_t>(s) * H + h) * kD + j) * W;
 #pragma unroll
     for (int t = 0; t < kMaxConvWidth; ++t) w[t] = t < W ? wv[t] : 0.f;
-    float* dst = s == 0 ? &sm.q[0][j] : (s == 1 ? &sm.k[0][j] : &sm.v[0][j]);
+    float* dst = s == 0 ? &sm.q[0][kp(j)] : (s == 1 ? &sm.k[0][kp(j)] : &sm.v[0][j]);
 #pragma unroll
     for (int i = 0; i < kMaxDecodeTokens; ++i) {
       float acc = 0.f;
@@ -140,7 +144,7 @@ __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, in
   for (int u = 0; u < 2; ++u) {
     const int i = half + 2 * u;
     if (i < n_tok) {
-      sm.alpha[i][j] = expf(fe.g_min * sigmoidf_(ea * zz[u]));
+      sm.alpha[i][kp(j)] = expf(fe.g_min * sigmoidf_(ea * zz[u]));
       if (fe.gate) sm.gw[i][j] = sigmoidf_(ga[u]) * gwt;
     }
   }
@@ -153,7 +157,7 @@ __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, in
     float qq = 0.f, kk = 0.f, kq = 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const float a = sm.q[warp][lane + 32 * m], c = sm.k[warp][lane + 32 * m];
+      const float a = sm.q[warp][kp(lane + 32 * m)], c = sm.k[warp][kp(lane + 32 * m)];
       qq = fmaf(a, a, qq); kk = fmaf(c, c, kk); kq = fmaf(a, c, kq);
     }
 #pragma unroll
@@ -165,8 +169,8 @@ __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, in
     const float sq = qq > 0.f ? 1.f / sqrtf(qq) : 0.f, sk = kk > 0.f ? 1.f / sqrtf(kk) : 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      sm.q[warp][lane + 32 * m] *= sq;
-      sm.k[warp][lane + 32 * m] *= sk;
+      sm.q[warp][kp(lane + 32 * m)] *= sq;
+      sm.k[warp][kp(lane + 32 * m)] *= sk;
     }
     if (lane == 0) sm.kq[warp] = kq * sq * sk;
   }
@@ -232,10 +236,10 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     for (int e = tid; e < n_tok * kD; e += kThreads) {
       const int i = e / kD, j = e - i * kD;
       const int64_t base = ((static_cast<int64_t>(b) * n_tok + i) * H + h) * kD + j;
-      sm.q[i][j] = __bfloat162float(q[base]);
-      sm.k[i][j] = __bfloat162float(k[base]);
+      sm.q[i][kp(j)] = __bfloat162float(q[base]);
+      sm.k[i][kp(j)] = __bfloat162float(k[base]);
       sm.v[i][j] = __bfloat162float(v[base]);
-      sm.alpha[i][j] = expf(g[base]);
+      sm.alpha[i][kp(j)] = expf(g[base]);
     }
     if (tid < n_tok) sm.beta[tid] = beta[(static_cast<int64_t>(b) * n_tok + tid) * H + h];
   }
@@ -244,7 +248,7 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     if (warp < n_tok) {  // k . q of token `warp` (the front end forms it with the normalisation)
       float acc = 0.f;
 #pragma unroll
-      for (int j = lane; j < kD; j += 32) acc += sm.k[warp][j] * sm.q[warp][j];
+      for (int j = lane; j < kD; j += 32) acc += sm.k[warp][kp(j)] * sm.q[warp][kp(j)];
 #pragma unroll
       for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (lane == 0) sm.kq[warp] = acc;
@@ -262,10 +266,19 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
   for (int i = 0; i < n_tok; ++i) {
     // X = Diag(alpha) S, then partial w = X^T k and p = X^T q over this thread's rows.
     uint64_t w01 = f32x2(0.f, 0.f), w23 = w01, p01 = w01, p23 = w01;
+    float av[kRowsPerThread], kv[kRowsPerThread], qv[kRowsPerThread];  // this thread's rows
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; j += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(&sm.alpha[i][r0 * 16 + j]);
+      const float4 k4 = *reinterpret_cast<const float4*>(&sm.k[i][r0 * 16 + j]);
+      const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[i][r0 * 16 + j]);
+      av[j] = a4.x; av[j + 1] = a4.y; av[j + 2] = a4.z; av[j + 3] = a4.w;
+      kv[j] = k4.x; kv[j + 1] = k4.y; kv[j + 2] = k4.z; kv[j + 3] = k4.w;
+      qv[j] = q4.x; qv[j + 1] = q4.y; qv[j + 2] = q4.z; qv[j + 3] = q4.w;
+    }
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) {
-      const int row = r0 + 8 * m;
-      const float a = sm.alpha[i][row], kk = sm.k[i][row], qq = sm.q[i][row];
+      const float a = av[m], kk = kv[m], qq = qv[m];
       const uint64_t a2 = f32x2(a, a), k2 = f32x2(kk, kk), q2 = f32x2(qq, qq);
       s2[m][0] = mul_f32x2(s2[m][0], a2);
       s2[m][1] = mul_f32x2(s2[m][1], a2);
@@ -306,7 +319,7 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     const uint64_t u01 = f32x2(u.x, u.y), u23 = f32x2(u.z, u.w);
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) {
-      const float kk = sm.k[i][r0 + 8 * m];
+      const float kk = kv[m];
       const uint64_t k2 = f32x2(kk, kk);
       s2[m][0] = fma_f32x2(k2, u01, s2[m][0]);
       s2[m][1] = fma_f32x2(k2, u23, s2[m][1]);
