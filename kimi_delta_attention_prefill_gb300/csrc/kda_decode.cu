@@ -64,7 +64,9 @@ struct DecodeSmemT<true> : DecodeSmem {
   float gw[kMaxDecodeTokens][kD];  // output stage: Sigmoid(gate) x weight
 };
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+// Front-end gates with the fast exponential and reciprocal (a few ulp: far inside the
+// step's 1e-4 tolerance); 1 + e^-x = inf for very negative x gives 0.
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 // Front end of one (sequence, head): projected inputs + cache -> sm.q, sm.k (unit rows),
 // sm.v, sm.alpha, sm.beta; the cache advanced by nc committed tokens (nc = 0: unchanged).
@@ -81,7 +83,7 @@ __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, in
   const int64_t tstride = static_cast<int64_t>(H) * kD;
   const int64_t tok_base = static_cast<int64_t>(b) * n_tok * tstride + static_cast<int64_t>(h) * kD + j;
   // gate inputs (independent of the convolution): tokens half and half + 2 of channel j
-  const float ea = expf(fe.a_log[h]);
+  const float ea = __expf(fe.a_log[h]);
   float zz[2];
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
@@ -144,7 +146,7 @@ __device__ void stage_front(DecodeSmemT<true>& sm, const FrontEnd& fe, int b, in
   for (int u = 0; u < 2; ++u) {
     const int i = half + 2 * u;
     if (i < n_tok) {
-      sm.alpha[i][kp(j)] = expf(fe.g_min * sigmoidf_(ea * zz[u]));
+      sm.alpha[i][kp(j)] = __expf(fe.g_min * sigmoidf_(ea * zz[u]));
       if (fe.gate) sm.gw[i][j] = sigmoidf_(ga[u]) * gwt;
     }
   }
