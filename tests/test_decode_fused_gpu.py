@@ -56,7 +56,7 @@ def check(x, o, S, cache, ref, bsel=None):
 
 
 @pytest.mark.parametrize("W,act", [(1, "none"), (2, "silu"), (3, "none"), (4, "none"), (4, "silu")])
-@pytest.mark.parametrize("n_tok,commit", [(1, "all"), (4, "random")])
+@pytest.mark.parametrize("n_tok,commit", [(1, "all"), (2, "random"), (3, "all"), (4, "random")])
 def test_fused_step_against_oracle(W, act, n_tok, commit):
     x = inputs.make_decode_frontend(6, n_tok, 3, W=W, seed=10 * W + n_tok, commit=commit)
     o, S, cache, st = run(x, act)
@@ -137,10 +137,12 @@ def test_verify_workload_sampled():
     assert np.array_equal(host(cache[bsel]), ref["conv_cache"])
 
 
-@pytest.mark.parametrize("z_val,b_val", [(30.0, 30.0), (-30.0, -30.0), (30.0, -30.0)])
+@pytest.mark.parametrize("z_val,b_val", [(30.0, 30.0), (-30.0, -30.0), (30.0, -30.0), (100.0, -100.0),
+                                         (-100.0, 100.0)])
 def test_saturated_gates(z_val, b_val):
     """z = +-30 puts the decay at g_min or 0 (alpha = e^-5 or 1), b = +-30 puts beta at 1 or
-    0: the gates' saturated ends, against the oracle."""
+    0: the gates' saturated ends, against the oracle.  At +-100, e^-x overflows fp32 in the
+    sigmoid's denominator (1 + e^100 = inf), which must give exactly 0, not a NaN."""
     x = inputs.make_decode_frontend(3, 4, 2, W=3, seed=54, commit="random")
     x.z.fill_(z_val)
     x.b.fill_(b_val)
