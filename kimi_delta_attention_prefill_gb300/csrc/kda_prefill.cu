@@ -370,9 +370,10 @@ __device__ void put_inv_beta(const float* WI, const float* beta, uint8_t* dst, i
       const float4 y = *reinterpret_cast<const float4*>(src + 4);
       v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
     }
-    st4(dst + sw128(t, 2 * s0), pack_half2(v[0] * beta[s0], v[1] * beta[s0 + 1]),
-        pack_half2(v[2] * beta[s0 + 2], v[3] * beta[s0 + 3]), pack_half2(v[4] * beta[s0 + 4], v[5] * beta[s0 + 5]),
-        pack_half2(v[6] * beta[s0 + 6], v[7] * beta[s0 + 7]));
+    const float4 b0 = *reinterpret_cast<const float4*>(beta + s0), b1 = *reinterpret_cast<const float4*>(beta + s0 + 4);
+    st4(dst + sw128(t, 2 * s0), half2_of(mul_f32x2(f32x2(v[0], v[1]), f32x2(b0.x, b0.y))),
+        half2_of(mul_f32x2(f32x2(v[2], v[3]), f32x2(b0.z, b0.w))), half2_of(mul_f32x2(f32x2(v[4], v[5]), f32x2(b1.x, b1.y))),
+        half2_of(mul_f32x2(f32x2(v[6], v[7]), f32x2(b1.z, b1.w))));
   }
 }
 
@@ -671,11 +672,14 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
         const int s0 = col - lo;
         if (is_l) {
           float* wr = reinterpret_cast<float*>(sm + SM_WL) + t * kLdw + s0;
+          const uint64_t bt2 = f32x2(bt, bt);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(wr + e) =
-                make_float4((s0 + e < t) ? bt * r[e] : 0.f, (s0 + e + 1 < t) ? bt * r[e + 1] : 0.f,
-                            (s0 + e + 2 < t) ? bt * r[e + 2] : 0.f, (s0 + e + 3 < t) ? bt * r[e + 3] : 0.f);
+          for (int e = 0; e < 16; e += 4) {
+            const float2 a = unpack_f32x2(mul_f32x2(f32x2(r[e], r[e + 1]), bt2));
+            const float2 b = unpack_f32x2(mul_f32x2(f32x2(r[e + 2], r[e + 3]), bt2));
+            *reinterpret_cast<float4*>(wr + e) = make_float4((s0 + e < t) ? a.x : 0.f, (s0 + e + 1 < t) ? a.y : 0.f,
+                                                             (s0 + e + 2 < t) ? b.x : 0.f, (s0 + e + 3 < t) ? b.y : 0.f);
+          }
         } else {
           float v[16];
 #pragma unroll
@@ -1024,11 +1028,14 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               float y[8];
+              const uint64_t sc2 = f32x2(scale, scale);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&f[8 * h + 4 * c + e]));
-                y[2 * e] = r[8 * c + 2 * e] * scale * ff.x;
-                y[2 * e + 1] = r[8 * c + 2 * e + 1] * scale * ff.y;
+                const float2 v = unpack_f32x2(mul_f32x2(mul_f32x2(f32x2(r[8 * c + 2 * e], r[8 * c + 2 * e + 1]), sc2),
+                                                        f32x2(ff.x, ff.y)));
+                y[2 * e] = v.x;
+                y[2 * e + 1] = v.y;
               }
               dst[c] = make_uint4(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]), pack_bf162(y[4], y[5]),
                                   pack_bf162(y[6], y[7]));
@@ -1075,8 +1082,12 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
           for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
         }
         if (next) {
+          const uint64_t al2 = f32x2(al_next, al_next);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] *= al_next;
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v = unpack_f32x2(mul_f32x2(f32x2(r[e], r[e + 1]), al2));
+            r[e] = v.x; r[e + 1] = v.y;
+          }
           tmem_st32(tmem + tl + kTS + g * 32, r);
         }
       }
