@@ -5,11 +5,13 @@ step of the computation runs in the CUDA kernels of ``libkda.so`` (sm_103a); the
 no CPU or PyTorch fallback, and a missing library raises ``KdaLibraryError``.
 
 Functions mirror the C entry points: :func:`prefill` (``kda_prefill``, or
-``kda_prefill_gated`` when gate logits are given),
-:func:`decode` (``kda_decode``), :func:`prefill_workspace_size`
-(``kda_prefill_workspace_size``), :func:`status_string` (``kda_status_string``).
-Tensors are torch CUDA tensors; the launch goes to the current torch stream unless
-``stream`` is given.
+``kda_prefill_gated`` when gate logits are given), :func:`prefill_paged`
+(``kda_prefill_paged``), :func:`prefill_host` (``kda_prefill_host``, host buffers),
+:func:`decode` (``kda_decode``), :func:`decode_paged` (``kda_decode_paged``),
+:func:`decode_fused` (``kda_decode_fused``), the workspace-size queries, and
+:func:`status_string` (``kda_status_string``).  Tensors are torch CUDA tensors (pinned
+host tensors for :func:`prefill_host`); the launch goes to the current torch stream
+unless ``stream`` is given.
 """
 from __future__ import annotations
 
