@@ -45,8 +45,8 @@ CPU_SAMPLE_TOKENS = 8192  # the whole workload: about 1.5 s on 16 host cores (ab
 # (both kernels' traffic grows in proportion to the heads); the capture and the command
 # that made it are summarised in profiles/.  Set to None when the kernel changes until it is
 # captured again.
-PREFILL_TRAFFIC_PER_HEAD = 189_440_512 // 16  # bytes per head of the 8192-token launch
-GATED_TRAFFIC_PER_HEAD = 225_265_152 // 16  # the same launch with the fused output stage
+PREFILL_TRAFFIC_PER_HEAD = 188_980_992 // 16  # bytes per head of the 8192-token launch
+GATED_TRAFFIC_PER_HEAD = 225_005_312 // 16  # the same launch with the fused output stage
 DECODE_TRAFFIC_PER_HEAD = 486_659_328 // 16  # bytes per head of the 256-sequence launch
 
 

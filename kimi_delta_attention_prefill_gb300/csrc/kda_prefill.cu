@@ -980,6 +980,55 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     }
     if (!kwait<kHook>(&bars[BAR_M34], n & 1)) ctrl[CTRL_ABORT] = 1;
     tc_fence_after();
+    // ---- state -> fp16 operand of the next chunk; checkpoint / final state in fp32; the
+    //      TMEM copy is decayed by the next chunk's a_last for its update (S <- Diag(a_last) S)
+    {
+      const bool next = n + 1 < n_chunks;
+      float al_next = 1.f;
+      if (next) {
+        if (!kwait<kHook>(&bars[BAR_AL], (n + 1) & 1)) ctrl[CTRL_ABORT] = 1;
+        al_next = alast[((n + 1) & 1) * 128 + i];
+      }
+      const int pos = min((cidx + 1) * kChunk, w.len);
+      float* ckdst = nullptr;
+      if (ck < w.ck_end && p.ckpt_pos[ck] == pos) {
+        const int64_t e = static_cast<int64_t>(ck) * p.H + w.h;
+        ckdst = p.pg.pool ? page_ptr(p, p.pg.ckpt, e) : p.ckpts + e * (kHeadDim * kHeadDim);
+        ++ck;
+      }
+      float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTS + g * 32, r);
+        uint8_t* dst = sm + SM_S16 + (g >> 1) * 16384;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st4(dst + sw128(i, 64 * (g & 1) + 16 * c), pack_half2(r[8 * c], r[8 * c + 1]),
+              pack_half2(r[8 * c + 2], r[8 * c + 3]), pack_half2(r[8 * c + 4], r[8 * c + 5]),
+              pack_half2(r[8 * c + 6], r[8 * c + 7]));
+        if (ckdst) {
+          float4* d4 = reinterpret_cast<float4*>(ckdst + i * kHeadDim + g * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        }
+        if (fin) {
+          float4* d4 = reinterpret_cast<float4*>(fin + i * kHeadDim + g * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        }
+        if (next) {
+          const uint64_t al2 = f32x2(al_next, al_next);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v = unpack_f32x2(mul_f32x2(f32x2(r[e], r[e + 1]), al2));
+            r[e] = v.x; r[e + 1] = v.y;
+          }
+          tmem_st32(tmem + tl + kTS + g * 32, r);
+        }
+      }
+      tmem_wait_st();
+    }
     // ---- outputs (rows in lanes 64-127)
     if (do_o && rw >= 2 && !gated) {
       const int t = tid - 64;
@@ -1043,55 +1092,6 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
           }
         }
       }
-    }
-    // ---- state -> fp16 operand of the next chunk; checkpoint / final state in fp32; the
-    //      TMEM copy is decayed by the next chunk's a_last for its update (S <- Diag(a_last) S)
-    {
-      const bool next = n + 1 < n_chunks;
-      float al_next = 1.f;
-      if (next) {
-        if (!kwait<kHook>(&bars[BAR_AL], (n + 1) & 1)) ctrl[CTRL_ABORT] = 1;
-        al_next = alast[((n + 1) & 1) * 128 + i];
-      }
-      const int pos = min((cidx + 1) * kChunk, w.len);
-      float* ckdst = nullptr;
-      if (ck < w.ck_end && p.ckpt_pos[ck] == pos) {
-        const int64_t e = static_cast<int64_t>(ck) * p.H + w.h;
-        ckdst = p.pg.pool ? page_ptr(p, p.pg.ckpt, e) : p.ckpts + e * (kHeadDim * kHeadDim);
-        ++ck;
-      }
-      float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float r[32];
-        tmem_ld32(tmem + tl + kTS + g * 32, r);
-        uint8_t* dst = sm + SM_S16 + (g >> 1) * 16384;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          st4(dst + sw128(i, 64 * (g & 1) + 16 * c), pack_half2(r[8 * c], r[8 * c + 1]),
-              pack_half2(r[8 * c + 2], r[8 * c + 3]), pack_half2(r[8 * c + 4], r[8 * c + 5]),
-              pack_half2(r[8 * c + 6], r[8 * c + 7]));
-        if (ckdst) {
-          float4* d4 = reinterpret_cast<float4*>(ckdst + i * kHeadDim + g * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
-        }
-        if (fin) {
-          float4* d4 = reinterpret_cast<float4*>(fin + i * kHeadDim + g * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
-        }
-        if (next) {
-          const uint64_t al2 = f32x2(al_next, al_next);
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 v = unpack_f32x2(mul_f32x2(f32x2(r[e], r[e + 1]), al2));
-            r[e] = v.x; r[e + 1] = v.y;
-          }
-          tmem_st32(tmem + tl + kTS + g * 32, r);
-        }
-      }
-      tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before();
