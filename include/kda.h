@@ -116,7 +116,9 @@ size_t kda_prefill_workspace_size(int n_seq, int H, int d, int64_t total_tokens,
  *   ckpts        [n_ckpt, H, d, d] fp32, slot j = checkpoint ckpt_pos[j] (write only)
  *   n_segments   0: the library splits long sequences by its own rule (a function of the
  *                sequence's own length, H and the SM count only, so a sequence gives the
- *                same bits packed or alone); k >= 1: split every sequence into
+ *                same bits packed or alone): the count with the least chain time when the
+ *                two passes run in waves of one CTA per SM, never two segments (they only
+ *                run one after the other); k >= 1: split every sequence into
  *                min(k, its chunk count) segments.
  *   workspace    device buffer of kda_prefill_workspace_size(...) bytes (may be NULL
  *                when that is 0), 256-byte aligned.
