@@ -48,6 +48,8 @@ CPU_SAMPLE_TOKENS = 8192  # the whole workload: about 1.5 s on 16 host cores (ab
 PREFILL_TRAFFIC_PER_HEAD = 188_980_992 // 16  # bytes per head of the 8192-token launch
 GATED_TRAFFIC_PER_HEAD = 225_005_312 // 16  # the same launch with the fused output stage
 DECODE_TRAFFIC_PER_HEAD = 486_659_328 // 16  # bytes per head of the 256-sequence launch
+VERIFY_TRAFFIC = {}  # n_tok -> bytes per 256 x 96 launch of the plain verify curve
+VARLEN_TRAFFIC = None  # bytes per launch of the varlen workload
 
 
 def load_peaks():
@@ -383,6 +385,56 @@ def run_ours(args, world, rank, local):
                           "kernel": "decode_kernel<front end>", "bytes_per_launch": f_bytes}}
     del fx, fS, fcache, fo
 
+    # the verify cost curve ("部署 Kimi K3 ..." section 4: verification grows sub-linearly in
+    # the tokens verified): plain kda_decode over 256 x 96 states with n_tok = 1..4 prepared
+    # tokens, every token committed; algorithmic bytes = the state read and write plus each
+    # token's inputs and outputs
+    verify_curve = []
+    for nt in (1, 2, 3, 4):
+        vx = inputs.make_decode(256, nt, H, seed=3, device=dev)
+        vS = vx.S0.clone()
+        vo = torch.empty((256, nt, H, D), dtype=torch.float32, device=dev)
+        vms = timed(lambda: kda.decode(vx.q, vx.k, vx.v, vx.g, vx.beta, vS, o=vo, stream=stream), dsteps)
+        v_bytes = n_units * (DECODE_STATE_BYTES + nt * DECODE_IO_BYTES)
+        verify_curve.append({"n_tok": nt, "us_per_step": vms * 1e3,
+                             "state_gbs": n_units * DECODE_STATE_BYTES / (vms / 1e3) / 1e9,
+                             "roofline": {"bound": "hbm", "achieved": v_bytes / (vms / 1e3) / 1e9,
+                                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": v_bytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                          "traffic": VERIFY_TRAFFIC.get(nt), "kernel": "decode_kernel",
+                                          "bytes_per_launch": v_bytes}})
+        del vx, vS, vo
+    verify = {"metric": "KDA verify step time vs tokens verified (256 x 96 heads, plain kda_decode, "
+                        "all tokens committed)", "unit": "us", "curve": verify_curve,
+              "cost_vs_one_token": [c["us_per_step"] / verify_curve[0]["us_per_step"] for c in verify_curve]}
+
+    # the varlen workload: 64 packed sequences of 512..16384 tokens, 96 heads, stress decay,
+    # nonzero entry states, a checkpoint every 512 tokens; algorithmic bytes = the tokens'
+    # inputs and outputs, the entry and final states and every checkpoint
+    vlx = inputs.make_workload("varlen", device=dev)
+    vT = vlx.q.shape[0]
+    vcu, voff, vpos = (t.to(dev) for t in (vlx.cu_seqlens, vlx.ckpt_off, vlx.ckpt_pos))
+    vlo = torch.empty_like(vlx.q)
+    vlS = torch.empty((vlx.n_seq, H, D, D), dtype=torch.float32, device=dev)
+    vlck = torch.empty((vlx.ckpt_pos.numel(), H, D, D), dtype=torch.float32, device=dev)
+    assert kda.prefill_workspace_size(vlx.n_seq, H, vT) == 0
+
+    def vlstep():
+        kda.prefill(vlx.q, vlx.k, vlx.v, vlx.g, vlx.beta, vcu, S_in=vlx.S0, ckpt_off=voff, ckpt_pos=vpos, o=vlo,
+                    S_out=vlS, ckpts=vlck, stream=stream)
+
+    vlms = timed(vlstep, 5)
+    vl_bytes = vT * H * PREFILL_BYTES_PER_TOKEN_HEAD + (2 * vlx.n_seq + vlx.ckpt_pos.numel()) * H * STATE_BYTES
+    varlen = {"metric": f"KDA varlen prefill tokens/s ({vlx.n_seq} packed sequences of 512..16384 tokens, "
+                        f"{vT} tokens, H=96, stress decay, entry states, {vlx.ckpt_pos.numel()} checkpoint "
+                        "positions every 512 tokens)",
+              "value": vT / (vlms / 1e3), "unit": "tokens/s", "ms_per_step": vlms,
+              "roofline": {"bound": "hbm", "achieved": vl_bytes / (vlms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": vl_bytes / (vlms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                           "traffic": VARLEN_TRAFFIC, "kernel": "prefill_kernel (one CTA per sequence and head)",
+                           "bytes_per_launch": vl_bytes}}
+    del vlx, vlo, vlS, vlck
+
     # end to end through the public host-buffer call (kda_prefill_host): every step uploads
     # its inputs from pinned host memory, computes, and downloads o and the final state;
     # the call pipelines the three over blocks of the token stream
@@ -446,6 +498,8 @@ def run_ours(args, world, rank, local):
             "paged": paged,
             "decode_fused": fused,
             "prefill_1m": long_prefill,
+            "varlen": varlen,
+            "verify": verify,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_prefill * args.steps,
             "clocks": clk.summary(),

@@ -14,7 +14,9 @@
  *  - d_k = d_v = d = 128 (KDA_HEAD_DIM); any other d returns KDA_ERR_UNSUPPORTED.
  *  - Every pointer argument is a DEVICE pointer on the current CUDA device, owned by
  *    the caller.  The library allocates no device memory and keeps no state between
- *    calls.  Tensor pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT otherwise).
+ *    calls, with two exceptions described at those calls: kda_prefill_noalloc's fixed
+ *    scratch array, and the streams and events kda_prefill_host keeps per device.  Tensor
+ *    pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT otherwise).
  *  - Calls are asynchronous on `stream`: they validate what the host can see, enqueue
  *    kernels and return.  A non-KDA_OK return means nothing was enqueued (except
  *    KDA_ERR_CUDA, returned when a launch itself failed).
@@ -282,8 +284,11 @@ kda_status kda_decode_fused(const kda_bf16* qp, const kda_bf16* kp, const kda_bf
  *                aligned: device copies of the inputs, o and the states
  * The call enqueues the work and returns: `stream` is made to wait for the last transfer, so
  * synchronising it (or an event recorded on it) means o and S_out are in host memory.  The
- * host buffers must stay valid until then.  Streams and events the call creates are released
- * by the driver once the work has finished.
+ * host buffers must stay valid until then.  The transfers run on two streams of the library's
+ * own, created with a set of events by the first call on each device and kept for the life
+ * of the process (not after cudaDeviceReset: do not call it on a device after a reset).
+ * Calls from several host threads are safe; their transfers share those streams and run in
+ * call order.
  */
 size_t kda_prefill_host_workspace_size(int n_seq, int H, int d, int64_t total_tokens, int64_t block_tokens);
 kda_status kda_prefill_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
@@ -323,11 +328,18 @@ void kda_debug_stall_next_prefill(int chunk);
  *
  *  - A problem whose kda_prefill_workspace_size(...) exceeds KDA_NOALLOC_SCRATCH_BYTES is
  *    rejected with KDA_ERR_WORKSPACE before anything is enqueued (the 1M-token, 8-head
- *    prefill with the library's own split needs about 30 MB; split counts forced through
- *    n_segments can need more).
- *  - The first call on each device, made while that device is current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call before any stream
- *    capture on the device.
+ *    prefill with the library's own split needs about 31.5 MB on a 152-SM GB300, and fits
+ *    up to 167 SMs; split counts forced through n_segments can need more).
+ *  - Set-up: the first call on each device, made while that device is current and whatever
+ *    the problem (an empty one, n_seq = 0, will do), looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it for the rest of the process.  Under the CUDA
+ *    runtime's default lazy module loading, that first call is also when the driver loads
+ *    the library code holding the array onto the device and reserves its 32 MiB.  Make the
+ *    first call during the caller's own set-up: before a framework claims the device's
+ *    memory, and before any stream capture on the device.  A failed look-up returns
+ *    KDA_ERR_CUDA and leaves no error pending in the runtime.
+ *  - The cached address does not survive cudaDeviceReset: after a reset of a device, do not
+ *    call kda_prefill_noalloc on it again in the same process.
  *  - Every call shares the one array and it keeps the previous call's contents (no part of
  *    it needs to start at zero: each call writes every entry it reads).  Calls whose work
  *    may overlap on the GPU -- on different streams, or from several host threads without

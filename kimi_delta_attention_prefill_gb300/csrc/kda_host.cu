@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "kda.h"
@@ -95,24 +96,35 @@ bool plan_blocks(const int32_t* cu, int n_seq, int64_t T, int64_t target, std::v
   return true;
 }
 
-struct Owned {  // streams and events of one call, released when it returns (the work may still run)
-  std::vector<cudaStream_t> streams;
-  std::vector<cudaEvent_t> events;
-  ~Owned() {
-    for (cudaEvent_t e : events) cudaEventDestroy(e);
-    for (cudaStream_t s : streams) cudaStreamDestroy(s);
-  }
-  cudaError_t stream(cudaStream_t* s) {
-    cudaError_t r = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
-    if (r == cudaSuccess) streams.push_back(*s);
-    return r;
-  }
-  cudaError_t event(cudaEvent_t* e) {
-    cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
-    if (r == cudaSuccess) events.push_back(*e);
+// Streams and events of the executor, per device, created by the first call on that device
+// and kept for the life of the process (a call used to create and destroy about 2 + 2 x
+// blocks of them).  A call holds the device's lock while it enqueues: an event is recorded
+// again only by a later call, after every wait on its previous record has been enqueued
+// (cudaStreamWaitEvent waits for the record current when it is called), so calls may
+// overlap on the GPU.  Two calls' transfers share the two streams and run in call order.
+constexpr int kMaxExecDevices = 64;
+struct ExecCache {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr, fail_up = nullptr, fail_down = nullptr;
+  cudaEvent_t landed[kMaxHostBlocks] = {}, computed[kMaxHostBlocks] = {};
+
+  cudaError_t init() {  // creates what is still missing (a failed earlier attempt keeps its part)
+    if (ready) return cudaSuccess;
+    cudaError_t r = cudaSuccess;
+    for (cudaStream_t* st : {&up, &down})
+      if (r == cudaSuccess && !*st) r = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+    auto ev = [&](cudaEvent_t* e) {
+      if (r == cudaSuccess && !*e) r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+    };
+    for (cudaEvent_t* e : {&start, &done, &fail_up, &fail_down}) ev(e);
+    for (int j = 0; j < kMaxHostBlocks; ++j) { ev(&landed[j]); ev(&computed[j]); }
+    if (r == cudaSuccess) ready = true;
     return r;
   }
 };
+ExecCache g_exec[kMaxExecDevices];
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -232,23 +244,24 @@ kda_status kda_prefill_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16
   }
   if (off > n_seq + 2 * kMaxHostBlocks) return KDA_ERR_UNSUPPORTED;
 
-  Owned own;
-  cudaStream_t up = nullptr, down = nullptr;
-  cudaEvent_t start = nullptr, done = nullptr;
-  if (own.stream(&up) != cudaSuccess || own.stream(&down) != cudaSuccess || own.event(&start) != cudaSuccess ||
-      own.event(&done) != cudaSuccess)
+  if (dev < 0 || dev >= kMaxExecDevices) return KDA_ERR_UNSUPPORTED;
+  ExecCache& ex = g_exec[dev];
+  std::lock_guard<std::mutex> lock(ex.mu);
+  if (ex.init() != cudaSuccess) {
+    cudaGetLastError();
     return KDA_ERR_CUDA;
-  std::vector<cudaEvent_t> landed(tab.n), computed(tab.n);
-  for (int j = 0; j < tab.n; ++j)
-    if (own.event(&landed[j]) != cudaSuccess || own.event(&computed[j]) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  cudaStream_t up = ex.up, down = ex.down;
+  cudaEvent_t start = ex.start, done = ex.done;
+  const cudaEvent_t* landed = ex.landed;
+  const cudaEvent_t* computed = ex.computed;
 
   // On a failure after the first enqueue, the work already queued on the two internal
   // streams may still run: the caller's stream is made to wait for it before returning, so
   // that synchronising `stream` still means no transfer touches the caller's buffers.
   auto fail = [&](kda_status code) {
-    cudaEvent_t e;
-    for (cudaStream_t sx : {up, down})
-      if (own.event(&e) == cudaSuccess && cudaEventRecord(e, sx) == cudaSuccess) cudaStreamWaitEvent(stream, e, 0);
+    if (cudaEventRecord(ex.fail_up, up) == cudaSuccess) cudaStreamWaitEvent(stream, ex.fail_up, 0);
+    if (cudaEventRecord(ex.fail_down, down) == cudaSuccess) cudaStreamWaitEvent(stream, ex.fail_down, 0);
     return code;
   };
   const size_t HD = static_cast<size_t>(H) * kHeadDim;

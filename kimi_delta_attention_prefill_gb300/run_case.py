@@ -23,6 +23,7 @@ def main():
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
     ap.add_argument("--tokens", type=int, default=None, help="override the length of a single-sequence prefill")
     ap.add_argument("--segments", type=int, default=0, help="prefill segment count (0 = library's choice)")
+    ap.add_argument("--n-tok", type=int, default=None, help="override the tokens of a decode / verify step")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--gated", action="store_true", help="prefill with the fused output stage")
     ap.add_argument("--fused", action="store_true",
@@ -35,6 +36,8 @@ def main():
         over["H"] = args.heads
     if args.tokens:
         over["lengths"] = [args.tokens]
+    if args.n_tok:
+        over["n_tok"] = args.n_tok
     x = inputs.make_workload(args.workload, device="cuda", **over)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     if inputs.WORKLOADS[args.workload]["kind"] == "decode":

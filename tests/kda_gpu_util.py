@@ -5,6 +5,7 @@ Tolerances (fixed by the acceptance bar for this path):
     prefill o      max|o - o_ref| / max|o_ref|            <= 1e-2   (bf16 output)
     prefill state  ||S - S_ref||_F / ||S_ref||_F          <= 1e-3   (final state, each checkpoint)
     decode o, S    max|x - x_ref| / max|x_ref|            <= 1e-4   (fp32 in and out)
+    output stage y the o bar carried through the stage plus y's rounding (``y_bound``)
 """
 from __future__ import annotations
 
@@ -38,6 +39,32 @@ def rel_max(x, ref):
 def rel_fro(x, ref):
     x, ref = np.asarray(x, np.float64), np.asarray(ref, np.float64)
     return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def y_bound(oref, gl, w, eps, omax):
+    """Allowed |y - y_ref| per element of the output stage y = sigmoid(a) w o~ / rms(o~)
+    ("Kimi K3.1 Pro 架构完全拆解" 3.3), for oracle rows ``oref`` [n, d] with gate logits ``gl``
+    and weight ``w``; ``omax`` = max|o~_ref| over the whole checked tensor.  Returns (bound,
+    y_ref).
+
+    The o bar admits any o~' with |o~' - o~_ref| <= eps_o = O_TOL omax per element.  In a row
+    of root mean square r (eps included) that moves y_c = s_c o~_c / r (s_c = sigmoid(a_c)
+    |w_c|) by at most s_c eps_o (1 + |o~_c| / r) / (r - eps_o) -- exactly, not to first
+    order: the numerator moves by at most eps_o and so does the root mean square (a norm).
+    A row within 2 eps_o of zero is inside the o bar's noise and may take any value a
+    normalised row can, |y_c| <= s_c sqrt(d).  y is then rounded to bf16 once (relative
+    error at most 2^-8), and fp32 arithmetic adds 1e-6 max|y_ref|."""
+    from oracle.epilogue import gated_rmsnorm, sigmoid
+    oref = np.asarray(oref, np.float64)
+    d = oref.shape[-1]
+    eps_o = O_TOL * float(omax)
+    s = sigmoid(gl) * np.abs(np.asarray(w, np.float64))
+    r = np.sqrt(np.mean(oref ** 2, axis=-1, keepdims=True) + eps)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        carried = s * eps_o * (1.0 + np.abs(oref) / r) / (r - eps_o)
+    carried = np.where(r > 2 * eps_o, carried, s * np.sqrt(d))
+    yr = gated_rmsnorm(oref, gl, w, eps)
+    return carried + 2.0 ** -8 * np.abs(yr) + 1e-6 * np.abs(yr).max(), yr
 
 
 def to_device(inp, device="cuda"):
