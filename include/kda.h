@@ -302,6 +302,40 @@ int kda_prefill_host_blocks(const int32_t* cu_seqlens, int n_seq, int64_t total_
                             int64_t* borders, int max_borders);
 
 /*
+ * Cross-device sequence split (KCP).  "部署 Kimi K3：从 KDA Kernel 到 Fleet 调度的推理 Infra
+ * 全景" section 2: a sequence's tokens are split over ranks in order; each rank summarises
+ * its token range by the pair (M, S~) -- the cumulative transition
+ * M = prod_t (I - beta_t k_t k_t^T) Diag(alpha_t) and the state S~ the range produces from a
+ * zero entry state -- so that its exit state for an entry state S is S~ + M S.  The ranks
+ * all-gather their pairs (a fixed 2 x 64 KiB per head, whatever the token count), each
+ * folds the pairs of the ranks before it onto the sequence's entry state, and runs its own
+ * range from the resulting true entry state with kda_prefill.  These two calls are the
+ * device parts; the exchange is the caller's (the Python binding's kcp module does it over
+ * torch.distributed).
+ *
+ * kda_prefill_pairs -- (M, S~) of every (sequence, head) over that sequence's rows.
+ *   q, k, v, g, beta, cu_seqlens, n_seq, total_tokens, H, d, dev_status: as kda_prefill
+ *   M, S_tilde   [n_seq, H, d, d] fp32 each (write only), row = d_k.  A sequence with no
+ *                rows gets M = I and S~ = 0.
+ * No workspace.  One chain per (sequence, head) for each of the two, on the prefill kernel.
+ */
+kda_status kda_prefill_pairs(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                             const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens, float* M,
+                             float* S_tilde, int H, int d, int* dev_status, cudaStream_t stream);
+
+/*
+ * kda_combine_pairs -- the entry state after n_pairs ranges, per (sequence, head):
+ *     E = S_in;  for r = 0 .. n_pairs - 1:  E = S~_r + M_r E;  entry = E
+ * (same page, section 2: the local sequential combine of the preceding ranks' pairs).
+ *   M, S_tilde   [n_pairs, n_seq, H, d, d] fp32 (may be NULL when n_pairs = 0)
+ *   S_in         [n_seq, H, d, d] fp32, or NULL for zeros
+ *   entry        [n_seq, H, d, d] fp32 (write only; must not overlap the inputs)
+ * fp32 arithmetic; n_pairs = 0 copies S_in.
+ */
+kda_status kda_combine_pairs(const float* M, const float* S_tilde, int n_pairs, const float* S_in, float* entry,
+                             int n_seq, int H, int d, cudaStream_t stream);
+
+/*
  * kda_debug_stall_next_prefill -- test hook for the bounded waits (no counterpart on the
  * pages).  The next prefill launch of this process runs a test instance of the kernel
  * whose prep warps withhold their first hand-off of chunk `chunk` (counted within each

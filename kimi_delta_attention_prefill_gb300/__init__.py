@@ -8,8 +8,10 @@ Functions mirror the C entry points: :func:`prefill` (``kda_prefill``, or
 ``kda_prefill_gated`` when gate logits are given), :func:`prefill_paged`
 (``kda_prefill_paged``), :func:`prefill_host` (``kda_prefill_host``, host buffers),
 :func:`decode` (``kda_decode``), :func:`decode_paged` (``kda_decode_paged``),
-:func:`decode_fused` (``kda_decode_fused``), the workspace-size queries, and
-:func:`status_string` (``kda_status_string``).  Tensors are torch CUDA tensors (pinned
+:func:`decode_fused` (``kda_decode_fused``), :func:`prefill_pairs` (``kda_prefill_pairs``),
+:func:`combine_pairs` (``kda_combine_pairs``), :func:`prefill_noalloc`
+(``kda_prefill_noalloc``), the workspace-size queries, and :func:`status_string`
+(``kda_status_string``).  The cross-device split's exchange is in :mod:`.kcp`.  Tensors are torch CUDA tensors (pinned
 host tensors for :func:`prefill_host`); the launch goes to the current torch stream
 unless ``stream`` is given.
 """
@@ -94,6 +96,10 @@ def library():
             if hasattr(lib, "kda_debug_stall_next_prefill"):  # diagnostic hook (tests)
                 lib.kda_debug_stall_next_prefill.restype = None
                 lib.kda_debug_stall_next_prefill.argtypes = [_c_int]
+            lib.kda_prefill_pairs.restype = _c_int
+            lib.kda_prefill_pairs.argtypes = [_vp] * 6 + [_c_int, _c_i64, _vp, _vp, _c_int, _c_int, _vp, _vp]
+            lib.kda_combine_pairs.restype = _c_int
+            lib.kda_combine_pairs.argtypes = [_vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _vp]
             lib.kda_prefill_noalloc.restype = _c_int
             lib.kda_prefill_noalloc.argtypes = ([_vp] * 7 + [_c_int, _c_i64] + [_vp, _vp, _c_i64] + [_vp] * 3 +
                                                 [_c_int, _c_int, _c_int, _vp, _vp])
@@ -502,3 +508,51 @@ def prefill_noalloc(q, k, v, g, beta, cu_seqlens, S_in=None, ckpt_off=None, ckpt
     if st != 0:
         raise KdaError(st, "kda_prefill_noalloc")
     return o, S_out, ckpts
+
+
+def prefill_pairs(q, k, v, g, beta, cu_seqlens, M=None, S_tilde=None, dev_status=None, stream=None):
+    """Per (sequence, head), the pair (M, S~) of the sequence's rows (``kda_prefill_pairs``):
+    the cumulative transition and the state from a zero entry state.  Inputs as
+    :func:`prefill`.  Returns ``(M, S_tilde)``, each ``[N, H, 128, 128]`` fp32."""
+    T, H, d = q.shape
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(g, "g", torch.float32, q.shape)
+    _need(beta, "beta", torch.float32, (T, H))
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seq = cu_seqlens.shape[0] - 1
+    if M is None:
+        M = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=q.device)
+    if S_tilde is None:
+        S_tilde = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=q.device)
+    _need(M, "M", torch.float32, (n_seq, H, d, d))
+    _need(S_tilde, "S_tilde", torch.float32, (n_seq, H, d, d))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32)
+    st = library().kda_prefill_pairs(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), n_seq, T,
+                                     _ptr(M), _ptr(S_tilde), H, d, _ptr(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_prefill_pairs")
+    return M, S_tilde
+
+
+def combine_pairs(M, S_tilde, S_in=None, entry=None, stream=None):
+    """Entry states after the ranges whose pairs are given (``kda_combine_pairs``): M and
+    S_tilde ``[R, N, H, 128, 128]`` fp32 (R >= 0), S_in ``[N, H, 128, 128]`` or None (zeros).
+    Returns ``entry`` ``[N, H, 128, 128]``: E = S_in, then E = S~_r + M_r E for r = 0 .. R-1."""
+    _need(M, "M", torch.float32)
+    if M.dim() != 5:
+        raise ValueError(f"M must have shape [R, N, H, d, d], got {tuple(M.shape)}")
+    R, n_seq, H, d, _ = M.shape
+    _need(S_tilde, "S_tilde", torch.float32, M.shape)
+    if S_in is not None:
+        _need(S_in, "S_in", torch.float32, (n_seq, H, d, d))
+    if entry is None:
+        entry = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=M.device)
+    _need(entry, "entry", torch.float32, (n_seq, H, d, d))
+    st = library().kda_combine_pairs(_ptr(M) if R else None, _ptr(S_tilde) if R else None, R, _ptr(S_in),
+                                     _ptr(entry), n_seq, H, d, _stream_handle(stream))
+    if st != 0:
+        raise KdaError(st, "kda_combine_pairs")
+    return entry

@@ -278,4 +278,41 @@ kda_status kda_decode_fused(const kda_bf16* qp, const kda_bf16* kp, const kda_bf
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_prefill_pairs(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const float* g,
+                             const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t total_tokens, float* M,
+                             float* S_tilde, int H, int d, int* dev_status, cudaStream_t stream) {
+  if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (n_seq < 0 || H < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0x7fffffffLL || static_cast<int64_t>(n_seq) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (n_seq == 0 || H == 0) return KDA_OK;
+  if (H > 65535 || n_seq > 0x7fffffff / 2) return KDA_ERR_UNSUPPORTED;  // grid: (2 n_seq, H)
+  if (!cu_seqlens || !M || !S_tilde) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !g || !beta)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(M, 16) ||
+      !aligned(S_tilde, 16) || !aligned(beta, 4) || !aligned(cu_seqlens, 4) || !aligned(dev_status, 4))
+    return KDA_ERR_ALIGNMENT;
+  kda_status st = current_device(nullptr);
+  if (st != KDA_OK) return st;
+  kda::PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens; a.n_seq = n_seq;
+  a.total_tokens = total_tokens; a.H = H; a.status = dev_status; a.stream = stream;
+  cudaError_t e = kda::launch_prefill_pairs(a, M, S_tilde);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_combine_pairs(const float* M, const float* S_tilde, int n_pairs, const float* S_in, float* entry,
+                             int n_seq, int H, int d, cudaStream_t stream) {
+  if (d != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (n_pairs < 0 || n_seq < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_seq) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (n_seq == 0 || H == 0) return KDA_OK;
+  if (H > 65535) return KDA_ERR_UNSUPPORTED;
+  if (!entry || (n_pairs > 0 && (!M || !S_tilde))) return KDA_ERR_INVALID_ARG;
+  if (!aligned(M, 16) || !aligned(S_tilde, 16) || !aligned(S_in, 16) || !aligned(entry, 16)) return KDA_ERR_ALIGNMENT;
+  kda_status st = current_device(nullptr);
+  if (st != KDA_OK) return st;
+  cudaError_t e = kda::launch_combine_pairs(M, S_tilde, n_pairs, S_in, entry, n_seq, H, stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -179,6 +179,13 @@ __host__ inline SplitLayout split_layout(int n_seq, int H, int64_t total_tokens,
 size_t prefill_workspace_bytes(int n_seq, int H, int64_t total_tokens, int n_segments, int num_sms);
 cudaError_t launch_prefill(const PrefillArgs& a, int num_sms);
 
+// Pair mode of the prefill kernel: per (sequence, head) the zero-entry state S~ and the
+// transition M of the sequence's rows, into [n_seq][H][128][128] each.
+cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde);
+// entry = fold over r < n_pairs of E <- S~_r + M_r E, from E = S_in (zeros when null).
+cudaError_t launch_combine_pairs(const float* M, const float* S_tilde, int n_pairs, const float* S_in, float* entry,
+                                 int n_seq, int H, cudaStream_t stream);
+
 // The split path's helper kernels (kda_segment.cu).
 cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, int num_sms);
 cudaError_t launch_split_scan(const PrefillArgs& a, const SplitLayout& L);

@@ -9,6 +9,13 @@
 //     U         = INV Diag(beta) (V - K_decay S)
 //     O         = Q_decay S + M_qk U
 //     S        <- Diag(a_last) S + K_restore^T U
+// computed here without forming U: with X = V - K_decay S (rounded to fp16 once),
+//     K_w = (INV Diag(beta))^T K_restore,   A_o = M_qk INV Diag(beta)
+//     O   = Q_decay S + A_o X,              S <- Diag(a_last) S + K_w^T X
+// (the same products, associated the other way round: K_restore^T (INV Diag(beta) X) =
+// K_w^T X).  Where the update telescopes over the chunk's tokens (repeated keys with
+// beta = 1: INV is I minus its first subdiagonal) the state sees X's one rounding instead
+// of one rounding per token of U.
 //
 // Decay range.  K_inv = K / a is not representable over 64 tokens (with g >= -5 the
 // cumulative log-decay reaches -320).  The pages bound the log-decay of a 16-token tile
@@ -30,8 +37,8 @@
 // Execution.  One CTA of 384 threads per work item, in two warp groups:
 //   recurrent (warps 0-3): the serial chain of chunk n -- X = V - K_decay S and
 //       Q_decay S (one product: the prep writes -K_decay, and V enters the accumulator
-//       through an identity operand held in TMEM), U, the state update and O -- on
-//       tcgen05 with the state resident in TMEM;
+//       through an identity operand held in TMEM), K_w and A_o, the state update and O --
+//       on tcgen05 with the state resident in TMEM;
 //   prep (warps 4-11): everything that does not depend on the state, for chunk n + 1 --
 //       loads, cumsum, decay factors, scaled operands, L / M_qk, INV -- so it overlaps
 //       the recurrence ("部署 Kimi K3 ..." 1.1: overlap the intra-chunk work with the
@@ -67,9 +74,10 @@ constexpr int kTotCg = 12, kTotPitch = 16 * kTotCg;
 
 // TMEM columns (all 128-lane layouts: lane = row of D).
 //   TS  [0, 128)   the state S, fp32 (lane = d_k row)
-//   TR1 [128, 256) lanes 0-63: X = V - K_decay S, then U; lanes 64-127: Q_decay S, then O
+//   TR1 [128, 256) lanes 0-63: X = V - K_decay S, then K_w; lanes 64-127: Q_decay S, then O
 //   TLM [256, 416) lanes 0-63: M_qk rows, lanes 64-127: L rows, 160 columns (4 blocks)
-//   TF  [416, 480) lanes 64-127: output-stage factors sigmoid(a) w, packed half2 (recurrent)
+//   TF  [416, 480) lanes 0-63: A_o = M_qk INV Diag(beta); lanes 64-127: output-stage factors
+//                  sigmoid(a) w, packed half2 (recurrent)
 //   TI  [480, 512) [I_64; 0] as bf16 pairs (lane = row, column = two K entries): the A
 //                  operand of the product that adds V to rows 0-63 of TR1
 constexpr uint32_t kTS = 0, kTR1 = 128, kTLM = 256, kTF = 416, kTI = 480;
@@ -78,10 +86,11 @@ __host__ __device__ constexpr uint32_t lm_col(int tb) { return tb == 0 ? 0u : tb
 // Shared memory (bytes from a 1024-aligned base).
 constexpr uint32_t SM_S16 = 0;        // S fp16, [i][j], 2 N-panels x 128 rows        (recurrent)
 constexpr uint32_t SM_KQ = 32768;     // [-K_decay; Q_decay] fp16, K-major, 2 x 128 rows (prep -> recurrent)
-constexpr uint32_t SM_V = 65536;      // v tiles (TMA), two stages of 16 KiB             (recurrent)
-constexpr uint32_t SM_XU = 98304;     // X, then U, fp16 [t][j], 2 N-panels x 64 rows    (recurrent)
-constexpr uint32_t SM_KR = 114688;    // K_restore fp16 [t][i], 2 M-panels x 64 rows     (prep -> recurrent)
-constexpr uint32_t SM_IM = 131072;    // [INV Diag(beta); M_qk] fp16, K-major, 128 rows  (prep -> recurrent)
+constexpr uint32_t SM_V = 65536;      // v tile (TMA), 16 KiB, one stage                 (recurrent)
+constexpr uint32_t SM_FREE = 81920;   // 16 KiB unused
+constexpr uint32_t SM_XU = 98304;     // X fp16 [t][j], 2 N-panels x 64 rows             (recurrent)
+constexpr uint32_t SM_KR = 114688;    // K_restore, then K_w, fp16 [t][i], 2 panels x 64 (prep -> recurrent)
+constexpr uint32_t SM_IM = 131072;    // [INV Diag(beta); M_qk, then A_o] fp16, 128 rows (prep -> recurrent)
 constexpr uint32_t SM_QAKA = 147456;  // [QA; KA] bf16, K-major, 2 x 128 rows            (prep)
 constexpr uint32_t SM_BT = 180224;    // B_0..B_3 bf16, K-major, 2 x 160 rows            (prep)
 constexpr uint32_t SM_MISC = 221184;
@@ -100,10 +109,10 @@ static_assert(SM_BT + 40960 == SM_MISC, "layout");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 enum {
-  BAR_V0 = 0, BAR_V1 = 1,  // v tile landed (TMA)
+  BAR_V0 = 0, BAR_SPARE = 1,  // v tile landed (TMA); index 1 unused
   BAR_LM = 2,              // L / M_qk product done (prep's MMA)
   BAR_M1 = 3,              // X = V - K_decay S, Q_decay S done
-  BAR_M2 = 4,              // U done
+  BAR_M2 = 4,              // K_w and A_o done
   BAR_M34 = 5,             // state update and O done
   BAR_KQ = 6,              // prep -> recurrent: [K_decay; Q_decay] of the chunk written
   BAR_IM = 7,              // prep -> recurrent: [INV Diag(beta); M_qk] written
@@ -150,6 +159,8 @@ struct KParams {
   const int4* items;      // work items (split path) or nullptr: item x = whole sequence x
   const int* item_count;  // device count of valid items
   float* slots;           // split-path state slots [slot][H][3][128][128]
+  float* pair_S;          // pair mode (no items): S~ of block 2 s, [n_seq][H][128][128]
+  float* pair_M;          //                      M  of block 2 s + 1, same layout
 };
 
 __device__ __forceinline__ void st4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -230,7 +241,7 @@ constexpr int kLdp = 20;  // row stride of the 16 x 16 scratch blocks
 
 // 16 x 16 x 16 block products on the warp's tensor path (mma.sync m16n8k8, tf32 operands
 // rounded to nearest, fp32 accumulation).  The operands carry 11 significant bits, the
-// precision INV keeps anyway once it is rounded to the fp16 operand of U = INV Diag(beta) X.
+// precision INV keeps anyway once INV Diag(beta) is rounded to its fp16 operand.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -707,12 +718,11 @@ __device__ void prep_group(const KParams& p, const Work& w, uint8_t* sm, uint64_
     // M_qk readers join at INV's first group-wide barrier
     if ((pw & 3) >= 2) named_bar_sync(kBarL, 128);
 
-    // ---- 5. INV = (I + L)^-1
+    // ---- 5. INV = (I + L)^-1 and INV Diag(beta) (rows 0..63 of [INV Diag(beta); M_qk]), and
+    //         K_restore: their buffers are free, since the M_qk readers waited for the previous
+    //         chunk's update before INV's group-wide barrier
     invert_unit_lower(reinterpret_cast<const float*>(sm + SM_WL), reinterpret_cast<float*>(sm + SM_WI),
                       reinterpret_cast<float*>(sm + SM_PT), ptid);
-
-    // ---- 6. INV Diag(beta) and K_restore (their buffers are free: the M_qk readers waited for
-    //         the previous chunk's update before INV's first group-wide barrier)
     put_inv_beta(reinterpret_cast<const float*>(sm + SM_WI), s_beta, sm + SM_IM, ptid);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -761,7 +771,7 @@ __device__ __forceinline__ void sigmoid_w_half2(const uint4& a8, const uint32_t 
 }
 
 // ------------------------------------------------------------- recurrent group
-// 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (P, then U)
+// 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (X, then K_w)
 // belong to warps 0-1, rows 64-127 (Q_decay S, then O) to warps 2-3; the state TS uses
 // all 128 lanes.
 template <bool kHook>
@@ -773,6 +783,11 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   const uint64_t dS16 = smem_desc(smem_u32(sm + SM_S16), 16384, 1024, kSwizzle128B);
   const uint64_t dKQ = smem_desc(smem_u32(sm + SM_KQ), 16, 1024, kSwizzle128B);
   const uint64_t dXU = smem_desc(smem_u32(sm + SM_XU), 8192, 1024, kSwizzle128B);
+  // INV Diag(beta) (rows 0..63 of SM_IM) read MN-major: as A it is (INV Diag(beta))^T (its
+  // second M panel, rows 64..127, is M_qk: masked lanes), as B it is INV Diag(beta) (N = 64)
+  const uint64_t dIT = smem_desc(smem_u32(sm + SM_IM), 8192, 1024, kSwizzle128B);
+  const uint64_t dMQ = smem_desc(smem_u32(sm + SM_IM + 8192), 16, 1024, kSwizzle128B);  // M_qk, K-major
+  const uint32_t id_ao = idesc_f16(128, 64, false, false, true);
   const uint64_t dKR = smem_desc(smem_u32(sm + SM_KR), 8192, 1024, kSwizzle128B);
   const uint64_t dIM = smem_desc(smem_u32(sm + SM_IM), 16, 1024, kSwizzle128B);
   const uint32_t id_k_mn = idesc_f16(128, 128, false, false, true);
@@ -816,14 +831,13 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     tmem_st32(tmem + tl + kTI, r);
   }
   tmem_wait_st();
-  if (tid == 0) {
-    for (int s = 0; s < 2 && s < n_chunks; ++s) {
-      mbar_arrive_expect_tx(&bars[BAR_V0 + s], 16384);
-      const int r0 = static_cast<int>(w.bos + static_cast<int64_t>(w.c0 + s) * kChunk);
-      tma_load_3d(sm + SM_V + s * 16384, &p.tm_v, &bars[BAR_V0 + s], 0, w.h, r0);
-      tma_load_3d(sm + SM_V + s * 16384 + 8192, &p.tm_v, &bars[BAR_V0 + s], 64, w.h, r0);
-    }
-  }
+  auto issue_v = [&](int cidx) {  // the v tile of chunk cidx into the one stage
+    mbar_arrive_expect_tx(&bars[BAR_V0], 16384);
+    const int r0 = static_cast<int>(w.bos + static_cast<int64_t>(cidx) * kChunk);
+    tma_load_3d(sm + SM_V, &p.tm_v, &bars[BAR_V0], 0, w.h, r0);
+    tma_load_3d(sm + SM_V + 8192, &p.tm_v, &bars[BAR_V0], 64, w.h, r0);
+  };
+  if (tid == 0) issue_v(w.c0);
   if (gated && tid < 64) {
     const float w0 = p.norm_weight ? p.norm_weight[2 * tid] : 1.f, w1 = p.norm_weight ? p.norm_weight[2 * tid + 1] : 1.f;
     reinterpret_cast<uint32_t*>(sm + SM_W)[tid] = pack_half2(w0, w1);
@@ -837,7 +851,6 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     const int cidx = w.c0 + n;
     const int64_t row0 = w.bos + static_cast<int64_t>(cidx) * kChunk;
     const int valid = min(kChunk, w.len - cidx * kChunk);
-    const int vs = n & 1;
     // the output stage's gate-logit rows of the next chunk, pulled into L2 a chunk ahead
     if (gated && rw >= 2 && n + 1 < n_chunks && kChunk + tid - 64 < w.len - cidx * kChunk) {
       const char* ar =
@@ -845,12 +858,6 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       prefetch_l2(ar);
       prefetch_l2(ar + 128);
       prefetch_l2(ar + 255);
-    }
-    if (tid == 0 && n >= 1 && n + 1 < n_chunks) {  // stage vs ^ 1 was consumed by the previous chunk's X
-      mbar_arrive_expect_tx(&bars[BAR_V0 + (vs ^ 1)], 16384);
-      const int r0 = static_cast<int>(row0 + kChunk);
-      tma_load_3d(sm + SM_V + (vs ^ 1) * 16384, &p.tm_v, &bars[BAR_V0 + (vs ^ 1)], 0, w.h, r0);
-      tma_load_3d(sm + SM_V + (vs ^ 1) * 16384 + 8192, &p.tm_v, &bars[BAR_V0 + (vs ^ 1)], 64, w.h, r0);
     }
 
     // ---- [X; Q_decay S] = [-K_decay; Q_decay] S + [I_64; 0] V (one M = 128 accumulator)
@@ -862,10 +869,10 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
         mma_f16(tmem + kTR1, dKQ + (((kk >> 2) * 16384 + 32 * (kk & 3)) >> 4), dS16 + ((kk * 2048) >> 4), id_k_mn,
                 kk > 0);
       // V enters rows 0-63 through the identity operand in TMEM (bf16, like the v tile)
-      if (!kwait<kHook>(&bars[BAR_V0 + vs], (n >> 1) & 1)) ctrl[CTRL_ABORT] = 1;
+      if (!kwait<kHook>(&bars[BAR_V0], n & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
       if (!v_zero) {
-        const uint64_t dV = smem_desc(smem_u32(sm + SM_V + vs * 16384), 8192, 1024, kSwizzle128B);
+        const uint64_t dV = smem_desc(smem_u32(sm + SM_V), 8192, 1024, kSwizzle128B);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_f16_ta(tmem + kTR1, tmem + kTI + 8 * kk, dV + ((kk * 2048) >> 4), id_v, 1);
       }
@@ -876,7 +883,10 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     if (rw < 2) {
       if (!kwait<kHook>(&bars[BAR_M1], n & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
-      if (tid == 0 && n + 1 < n_chunks) issue_qk(p, w, sm, bars, cidx + 1);  // the buffer is free again
+      if (tid == 0 && n + 1 < n_chunks) {  // the product has read both buffers: the next chunk's tiles
+        issue_qk(p, w, sm, bars, cidx + 1);
+        issue_v(cidx + 1);
+      }
       {
         const int t = tid;
         const bool mk = t < valid;
@@ -899,32 +909,59 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       tc_fence_before();
       named_bar_sync(kBarXU, 64);
 
-      // ---- U = INV Diag(beta) X (lanes 64-127 keep Q_decay S)
+      // ---- The chunk's INV Diag(beta) folded into the operands that would read U = INV Diag(beta) X:
+      //          K_w = (INV Diag(beta))^T K_restore   (S += K_restore^T U = K_w^T X)
+      //          A_o = M_qk INV Diag(beta)             (O += M_qk U = A_o X)
+      //      so the state and output products take X directly.  K_w lands in lanes 0-63 of TR1
+      //      (X is already in shared memory), A_o in lanes 0-63 of TF; both are read back as
+      //      fp16 over the operands they replace (K_restore, M_qk), which the products have read.
+      //      X is rounded to fp16 once, and where the update telescopes (repeated keys) the
+      //      state sees that one rounding instead of one per token of U.
       if (tid == 0) {
         if (!kwait<kHook>(&bars[BAR_IM], n & 1)) ctrl[CTRL_ABORT] = 1;
+        if (!kwait<kHook>(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), dXU + ((kk * 2048) >> 4), id_k_mn, kk > 0, 0u, 0u,
+          mma_f16_masked(tmem + kTR1, dIT + ((kk * 2048) >> 4), dKR + ((kk * 2048) >> 4), id_mn_mn, kk > 0, 0u, 0u,
                          0xffffffffu, 0xffffffffu);
+        if (do_o) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_masked(tmem + kTF, dMQ + ((32 * kk) >> 4), dIT + ((kk * 2048) >> 4), id_ao, kk > 0, 0u, 0u,
+                           0xffffffffu, 0xffffffffu);
+        }
         mma_commit(&bars[BAR_M2]);
       }
       if (!kwait<kHook>(&bars[BAR_M2], n & 1)) ctrl[CTRL_ABORT] = 1;
       tc_fence_after();
       {
-        const int t = tid;
-        const bool mk = t < valid;
+        const int t = tid;  // row of K_w (token s) and of A_o (token t)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           float r[32];
           tmem_ld32(tmem + tl + kTR1 + g * 32, r);
-          uint8_t* up = sm + SM_XU + (g >> 1) * 8192;
+          uint8_t* kp = sm + SM_KR + (g >> 1) * 8192;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float* x = r + 8 * c;
-            st4(up + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(mk ? x[0] : 0.f, mk ? x[1] : 0.f),
-                pack_half2(mk ? x[2] : 0.f, mk ? x[3] : 0.f), pack_half2(mk ? x[4] : 0.f, mk ? x[5] : 0.f),
-                pack_half2(mk ? x[6] : 0.f, mk ? x[7] : 0.f));
+            st4(kp + sw128(t, 64 * (g & 1) + 16 * c), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]),
+                pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+          }
+          asm volatile("" ::: "memory");
+        }
+        if (do_o) {
+          uint8_t* ap = sm + SM_IM + 8192;  // rows 64..127 share the swizzle phase of rows 0..63
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float r[32];
+            tmem_ld32(tmem + tl + kTF + g * 32, r);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float* x = r + 8 * c;
+              st4(ap + sw128(t, 64 * g + 16 * c), pack_half2(x[0], x[1]), pack_half2(x[2], x[3]),
+                  pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+            }
           }
         }
       }
@@ -932,16 +969,15 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       tc_fence_before();
       named_bar_sync(kBarXU, 64);
 
-      // ---- S += K_restore^T U ; O += M_qk U (lanes 0-63 untouched)
+      // ---- S += K_w^T X ; O += A_o X (lanes 0-63 untouched)
       if (tid == 0) {
-        if (!kwait<kHook>(&bars[BAR_KR], n & 1)) ctrl[CTRL_ABORT] = 1;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ud = dXU + ((kk * 2048) >> 4);
-          mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), ud, id_mn_mn, 1);
+          const uint64_t xd = dXU + ((kk * 2048) >> 4);
+          mma_f16(tmem + kTS, dKR + ((kk * 2048) >> 4), xd, id_mn_mn, 1);
           if (do_o)
-            mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), ud, id_k_mn, 1, 0xffffffffu, 0xffffffffu, 0u, 0u);
+            mma_f16_masked(tmem + kTR1, dIM + ((32 * kk) >> 4), xd, id_k_mn, 1, 0xffffffffu, 0xffffffffu, 0u, 0u);
         }
         mma_commit(&bars[BAR_M34]);
       }
@@ -1112,6 +1148,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (p.items) {
     if (static_cast<int>(blockIdx.x) >= *p.item_count) return;
     it = p.items[blockIdx.x];
+  } else if (p.pair_S) {  // pair mode: blocks 2 s and 2 s + 1 give S~ and M of sequence s
+    it = make_int4(static_cast<int>(blockIdx.x >> 1), 0, -1, (blockIdx.x & 1) ? kModeTrans : kModeZero);
   } else {
     it = make_int4(static_cast<int>(blockIdx.x), 0, -1, kModeFull);
   }
@@ -1151,8 +1189,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     switch (mode) {
       case kModeFirst: w.entry = s_in; w.s_out = slot_buf(0); break;
-      case kModeZero: w.entry = nullptr; w.s_out = slot_buf(0); break;
-      case kModeTrans: w.entry = nullptr; w.s_out = slot_buf(1); break;
+      case kModeZero: w.entry = nullptr; w.s_out = p.pair_S ? p.pair_S + unit * (kHeadDim * kHeadDim) : slot_buf(0); break;
+      case kModeTrans: w.entry = nullptr; w.s_out = p.pair_M ? p.pair_M + unit * (kHeadDim * kHeadDim) : slot_buf(1); break;
       case kModeTail: w.entry = slot_buf(2); w.s_out = (w.c1 == nch) ? s_out : nullptr; break;
       default: w.entry = s_in; w.s_out = s_out; break;
     }
@@ -1165,10 +1203,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   }
 
-  // ---- empty sequence: the final state is the entry state
+  // ---- empty sequence: the final state is the entry state (the transition of no tokens is I)
   if (w.c1 <= w.c0) {
     if (w.s_out)
-      for (int e = tid; e < kHeadDim * kHeadDim; e += kThreads) w.s_out[e] = w.entry ? w.entry[e] : 0.f;
+      for (int e = tid; e < kHeadDim * kHeadDim; e += kThreads)
+        w.s_out[e] = entry_identity ? (e / kHeadDim == e % kHeadDim ? 1.f : 0.f) : (w.entry ? w.entry[e] : 0.f);
     return;
   }
 
@@ -1205,6 +1244,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 }
 
 // ------------------------------------------------------------------- host side
+// The shared-memory opt-in is a per-device attribute of the function: set once per device.
+cudaError_t set_smem_attr() {
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit, std::memory_order_release);
+  }
+  return cudaSuccess;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -1235,6 +1290,26 @@ bool make_map(CUtensorMap* m, const void* base, bool is_f32, int H, int64_t T) {
 
 }  // namespace
 
+cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde) {
+  KParams p;
+  memset(&p, 0, sizeof(p));
+  const int64_t T = a.total_tokens;
+  if (T > 0) {
+    if (!make_map(&p.tm_q, a.q, false, a.H, T) || !make_map(&p.tm_k, a.k, false, a.H, T) ||
+        !make_map(&p.tm_v, a.v, false, a.H, T) || !make_map(&p.tm_g, a.g, true, a.H, T))
+      return cudaErrorInvalidValue;
+  }
+  p.q = static_cast<const __nv_bfloat16*>(a.q); p.k = static_cast<const __nv_bfloat16*>(a.k); p.g = a.g;
+  p.beta = a.beta; p.cu = a.cu_seqlens; p.status = a.status; p.stall_chunk = -1;
+  p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T;
+  p.pair_S = S_tilde; p.pair_M = M;
+  cudaError_t e = set_smem_attr();
+  if (e != cudaSuccess) return e;
+  prefill_kernel<false><<<dim3(2u * static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
+                          a.stream>>>(p);
+  return cudaGetLastError();
+}
+
 size_t prefill_workspace_bytes(int n_seq, int H, int64_t total_tokens, int n_segments, int num_sms) {
   return split_layout(n_seq, H, total_tokens, n_segments, num_sms).bytes;
 }
@@ -1255,18 +1330,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.pg = a.pages;
   p.stall_chunk = a.stall_chunk;
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
-  // the shared-memory opt-in is a per-device attribute of the function: set it once per device
-  static std::atomic<uint64_t> attr_set{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
-  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
-  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set.fetch_or(bit, std::memory_order_release);
-  }
+  cudaError_t e0 = set_smem_attr();
+  if (e0 != cudaSuccess) return e0;
   // the test hook's instance only when kda_debug_stall_next_prefill armed this launch
   auto kernel = a.stall_chunk >= 0 ? prefill_kernel<true> : prefill_kernel<false>;
   const SplitLayout L = split_layout(a.n_seq, a.H, T, a.n_segments, num_sms);

@@ -126,7 +126,67 @@ __global__ void __launch_bounds__(kScanThreads) split_scan_kernel(const int2* __
   }
 }
 
+// Cross-device KCP combine ("部署 Kimi K3 ..." section 2: after the all-gather, a rank
+// folds the preceding ranks' pairs in order): one CTA per (sequence, head, 16-column
+// block), E <- S~_r + M_r E for r = 0 .. n_pairs - 1 from E = S_in, fp32.
+__global__ void __launch_bounds__(kScanThreads) combine_pairs_kernel(const float* __restrict__ M,
+                                                                     const float* __restrict__ St, int n_pairs,
+                                                                     const float* __restrict__ S_in,
+                                                                     float* __restrict__ entry, int n_seq, int H) {
+  const int s = blockIdx.x, h = blockIdx.y, c_base = blockIdx.z * kScanCols;
+  const int64_t unit = static_cast<int64_t>(s) * H + h, units = static_cast<int64_t>(n_seq) * H;
+  __shared__ float E[kHeadDim][kScanCols];
+  const int tid = threadIdx.x, i = tid >> 1, c0 = (tid & 1) * 8;
+  {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (S_in) {
+      const float* x0 = S_in + unit * kStateFloats + i * kHeadDim + c_base + c0;
+      a = *reinterpret_cast<const float4*>(x0);
+      b = *reinterpret_cast<const float4*>(x0 + 4);
+    }
+    *reinterpret_cast<float4*>(&E[i][c0]) = a;
+    *reinterpret_cast<float4*>(&E[i][c0 + 4]) = b;
+  }
+  __syncthreads();
+  for (int r = 0; r < n_pairs; ++r) {
+    const int64_t base = (static_cast<int64_t>(r) * units + unit) * kStateFloats;
+    const float* Sr = St + base + i * kHeadDim + c_base + c0;
+    const float* Mrow = M + base + i * kHeadDim;
+    float acc[8];
+    {
+      const float4 a = *reinterpret_cast<const float4*>(Sr), b = *reinterpret_cast<const float4*>(Sr + 4);
+      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+    }
+#pragma unroll 4
+    for (int m4 = 0; m4 < kHeadDim; m4 += 4) {
+      const float4 mv = *reinterpret_cast<const float4*>(Mrow + m4);
+      const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 e0 = *reinterpret_cast<const float4*>(&E[m4 + u][c0]);
+        const float4 e1 = *reinterpret_cast<const float4*>(&E[m4 + u][c0 + 4]);
+        acc[0] += mm[u] * e0.x; acc[1] += mm[u] * e0.y; acc[2] += mm[u] * e0.z; acc[3] += mm[u] * e0.w;
+        acc[4] += mm[u] * e1.x; acc[5] += mm[u] * e1.y; acc[6] += mm[u] * e1.z; acc[7] += mm[u] * e1.w;
+      }
+    }
+    __syncthreads();  // every thread has read E
+    *reinterpret_cast<float4*>(&E[i][c0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(&E[i][c0 + 4]) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncthreads();
+  }
+  float* dst = entry + unit * kStateFloats + i * kHeadDim + c_base + c0;
+  *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(&E[i][c0]);
+  *reinterpret_cast<float4*>(dst + 4) = *reinterpret_cast<const float4*>(&E[i][c0 + 4]);
+}
+
 }  // namespace
+
+cudaError_t launch_combine_pairs(const float* M, const float* S_tilde, int n_pairs, const float* S_in, float* entry,
+                                 int n_seq, int H, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(n_seq), static_cast<unsigned>(H), kHeadDim / kScanCols);
+  combine_pairs_kernel<<<grid, kScanThreads, 0, stream>>>(M, S_tilde, n_pairs, S_in, entry, n_seq, H);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, int num_sms) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
