@@ -40,16 +40,18 @@ DECODE_STATE_BYTES = 8 * D * D
 DECODE_IO_BYTES = 3 * 2 * D + 4 * D + 4 + 4 * D
 DECODE_FLOP = 7 * D * D
 CPU_SAMPLE_TOKENS = 8192  # the whole workload: about 1.5 s on 16 host cores (about 20 s of CPU work)
-# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the kernels timed here, taken on a 16-head case and scaled by the units processed
-# (both kernels' traffic grows in proportion to the heads); the capture and the command
-# that made it are summarised in profiles/.  Set to None when the kernel changes until it is
-# captured again.
-PREFILL_TRAFFIC_PER_HEAD = 188_980_992 // 16  # bytes per head of the 8192-token launch
-GATED_TRAFFIC_PER_HEAD = 225_005_312 // 16  # the same launch with the fused output stage
-DECODE_TRAFFIC_PER_HEAD = 486_659_328 // 16  # bytes per head of the 256-sequence launch
-VERIFY_TRAFFIC = {}  # n_tok -> bytes per 256 x 96 launch of the plain verify curve
-VARLEN_TRAFFIC = None  # bytes per launch of the varlen workload
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of each launch timed here, at the benched shapes and inputs (no scaling); the
+# captures and the commands that made them are summarised in profiles/.  None when the
+# kernel changed after the counters were taken, until it is captured again.
+PREFILL_TRAFFIC = 1_197_215_488  # 8192 x 96 prefill launch
+GATED_TRAFFIC = 1_401_074_176    # the same with the fused output stage
+SPLIT_1M_TRAFFIC = 23_920_108_800  # 2^20 x 8 split prefill: both prefill passes together
+VARLEN_TRAFFIC = 98_669_809_408   # varlen workload launch
+DECODE_TRAFFIC = 3_208_086_528  # 256 x 96 decode launch, one token
+VERIFY_TRAFFIC = {1: 3_208_086_528, 2: 3_252_609_792, 3: 3_297_113_344, 4: 3_341_763_328}  # plain verify, n_tok
+PAGED_DECODE_TRAFFIC = 3_215_622_912  # 256 x 96 decode from scattered pages (page check kernels not included)
+FUSED_TRAFFIC = 3_297_246_976    # 256 x 96 fused verify launch
 
 
 def load_peaks():
@@ -264,7 +266,7 @@ def run_ours(args, world, rank, local):
              "unit": "tokens/s", "ms_per_step": gms,
              "roofline": {"bound": "hbm", "achieved": g_bytes / (gms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                           "unit": "GB/s", "frac": g_bytes / (gms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                          "traffic": None if GATED_TRAFFIC_PER_HEAD is None else GATED_TRAFFIC_PER_HEAD * H,
+                          "traffic": GATED_TRAFFIC,
                           "kernel": "prefill_kernel (gated)", "bytes_per_launch": g_bytes}}
 
     # decode: 256 sequences x 96 heads, one token; state stream against HBM
@@ -330,7 +332,7 @@ def run_ours(args, world, rank, local):
              "value": pd_gbs, "unit": "GB/s", "us_per_step": pdms * 1e3, "vs_contiguous": dms / pdms,
              "roofline": {"bound": "hbm", "achieved": dec_bytes / (pdms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                           "unit": "GB/s", "frac": dec_bytes / (pdms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                          "traffic": None, "kernel": "decode_kernel (paged) + page check",
+                          "traffic": PAGED_DECODE_TRAFFIC, "kernel": "decode_kernel (paged) + page check",
                           "bytes_per_launch": dec_bytes},
              "prefill": {"metric": "KDA paged prefill tokens/s (8192 x 96, entry and final states in pages)",
                          "value": T / (ppms / 1e3), "unit": "tokens/s", "ms_per_step": ppms,
@@ -356,7 +358,7 @@ def run_ours(args, world, rank, local):
                     "value": mT / (mms / 1e3), "unit": "tokens/s", "ms_per_step": mms,
                     "roofline": {"bound": "hbm", "achieved": m_bytes / (mms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": m_bytes / (mms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                                 "traffic": None, "kernel": "prefill_kernel (split: pass 1, scan, pass 3)",
+                                 "traffic": SPLIT_1M_TRAFFIC, "kernel": "prefill_kernel (split: pass 1, scan, pass 3)",
                                  "bytes_per_launch": m_bytes}}
     del mx, mo, mS, mws
 
@@ -365,7 +367,8 @@ def run_ours(args, world, rank, local):
     # bytes per (sequence, head): the state read and write, per token the projected inputs
     # (3 x 2d), z (4d), the beta logit, the gate logits (2d) and o (4d), and the
     # convolution cache read and write (2 x 3 x (W - 1) x d x 4)
-    fx = inputs.make_decode_frontend(256, 4, H, W=4, seed=6, commit="random", device=dev)
+    fx = inputs.make_decode_frontend(256, 4, H, W=4, seed=inputs.WORKLOADS["verify"]["seed"], commit="random",
+                                     device=dev)
     fS = fx.S0.clone()
     fcache = fx.conv_cache.clone()
     fo = torch.empty((256, 4, H, D), dtype=torch.float32, device=dev)
@@ -381,7 +384,7 @@ def run_ours(args, world, rank, local):
                        "conv width 4 + SiLU, L2 norm, gates, output stage), state GB/s",
              "value": n_units * DECODE_STATE_BYTES / (fms / 1e3) / 1e9, "unit": "GB/s", "us_per_step": fms * 1e3,
              "roofline": {"bound": "hbm", "achieved": f_bytes / (fms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                          "unit": "GB/s", "frac": f_bytes / (fms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                          "unit": "GB/s", "frac": f_bytes / (fms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": FUSED_TRAFFIC,
                           "kernel": "decode_kernel<front end>", "bytes_per_launch": f_bytes}}
     del fx, fS, fcache, fo
 
@@ -482,7 +485,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": None if PREFILL_TRAFFIC_PER_HEAD is None else PREFILL_TRAFFIC_PER_HEAD * H,
+                         "traffic": PREFILL_TRAFFIC,
                          "kernel": "prefill_kernel", "bytes_per_launch": alg_bytes,
                          "peak_source": peaks["source"],
                          "tensor": {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -492,7 +495,7 @@ def run_ours(args, world, rank, local):
                        "unit": "GB/s", "us_per_step": dms * 1e3,
                        "roofline": {"bound": "hbm", "achieved": dec_all_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": dec_all_gbs / peaks["hbm_gbs"],
-                                    "traffic": None if DECODE_TRAFFIC_PER_HEAD is None else DECODE_TRAFFIC_PER_HEAD * H,
+                                    "traffic": DECODE_TRAFFIC,
                                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes}},
             "gated": gated,
             "paged": paged,

@@ -69,7 +69,7 @@ def main():
         S0 = x.S0
         kw = {}
         if args.gated:
-            gate, w = inputs.make_output_stage(x.q.shape[0], x.q.shape[1], device="cuda")
+            gate, w = inputs.make_output_stage(x.q.shape[0], x.q.shape[1], seed=1, device="cuda")
             kw = dict(gate=gate, norm_weight=w)
         run = lambda: kda.prefill(x.q, x.k, x.v, x.g, x.beta, cu, S_in=S0, ckpt_off=off, ckpt_pos=pos,
                                   n_segments=args.segments, dev_status=status, **kw)
