@@ -48,10 +48,10 @@ PREFILL_TRAFFIC = 1_197_215_488  # 8192 x 96 prefill launch
 GATED_TRAFFIC = 1_401_074_176    # the same with the fused output stage
 SPLIT_1M_TRAFFIC = 23_920_108_800  # 2^20 x 8 split prefill: both prefill passes together
 VARLEN_TRAFFIC = 98_669_809_408   # varlen workload launch
-DECODE_TRAFFIC = 3_208_086_528  # 256 x 96 decode launch, one token
-VERIFY_TRAFFIC = {1: 3_208_086_528, 2: 3_252_609_792, 3: 3_297_113_344, 4: 3_341_763_328}  # plain verify, n_tok
-PAGED_DECODE_TRAFFIC = 3_215_622_912  # 256 x 96 decode from scattered pages (page check kernels not included)
-FUSED_TRAFFIC = 3_297_246_976    # 256 x 96 fused verify launch
+DECODE_TRAFFIC = None  # 256 x 96 decode launch, one token
+VERIFY_TRAFFIC = {}  # plain verify, n_tok -> bytes
+PAGED_DECODE_TRAFFIC = None  # 256 x 96 decode from scattered pages (page check kernels not included)
+FUSED_TRAFFIC = None  # 256 x 96 fused verify launch
 
 
 def load_peaks():

@@ -8,6 +8,11 @@
 // registers and only the state after the accepted prefix is written back
 // ("Kimi K3.1 Pro 架构完全拆解" 3.4).
 //
+// Latency: each CTA, once its own state loads are in flight, prefetches into L2 the state
+// and token inputs of the unit about half a resident wave ahead (one bulk prefetch of the
+// 64 KiB state, line prefetches of the inputs), so the loads of later CTAs (and the paged
+// decode's loads behind its page-table read) find their data in L2.
+//
 // Work split: one CTA of 256 threads per (sequence, head).  Warp w owns state columns
 // [16w, 16w + 16); lane = 4 r + c holds columns 16w + 4c .. +3 (one float4) of the 16
 // rows r, r + 8, ..., r + 120.  A warp therefore reads 8 rows x 64 contiguous bytes
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
               const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
               float* __restrict__ S, const int32_t* __restrict__ n_commit, float* __restrict__ o, int n_tok,
-              int H, int* __restrict__ status, const PageTables pg, const FrontEnd fe) {
+              int H, int* __restrict__ status, const PageTables pg, const FrontEnd fe, int lookahead) {
   __shared__ DecodeSmemT<kFront> sm;
   const int unit = blockIdx.x;  // b * H + h
   const int b = unit / H, h = unit - b * H;
@@ -226,6 +231,48 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
 #pragma unroll
   for (int m = 0; m < kRowsPerThread; ++m)
     s[m] = Sin ? Sin[((r0 + 8 * m) * kD + col) >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+  // The unit `lookahead` CTAs ahead (about half the resident CTAs) into L2: its state with
+  // one bulk prefetch (warp 1, lane 0; paged: behind its page-table read), its token inputs
+  // (and, with the front end, its convolution cache) line by line (warp 1), so that CTA's
+  // loads find them there.  A hint only: nothing depends on it for correctness.
+  if (warp == 1 && lookahead > 0) {
+    const int64_t nu = static_cast<int64_t>(unit) + lookahead;
+    if (nu < static_cast<int64_t>(gridDim.x)) {
+      if (lane == 0) {
+        const float* nxt = nullptr;
+        if (pg.pool) {
+          const int32_t np = pg.in ? pg.in[nu] : -1;
+          if (np >= 0 && np < pg.n_pages) nxt = pg.pool + static_cast<int64_t>(np) * kStateFloats;
+        } else {
+          nxt = S + nu * kStateFloats;
+        }
+        if (nxt) bulk_prefetch_l2(nxt, static_cast<uint32_t>(kStateFloats * sizeof(float)));
+      }
+      const int nb = static_cast<int>(nu / H), nh = static_cast<int>(nu - static_cast<int64_t>(nb) * H);
+      // lane = (token i, piece c): 8 pieces of 128 bytes cover a token's bf16 rows (2 each for
+      // three tensors) and its fp32 row (the remaining pieces, over 512 bytes)
+      for (int e = lane; e < n_tok * 8; e += 32) {
+        const int i = e >> 3, c = e & 7;
+        const int64_t row = ((static_cast<int64_t>(nb) * n_tok + i) * H + nh) * kD;
+        const char* ptr;
+        if constexpr (kFront) {
+          const char* b16 = static_cast<const char*>(c < 2 ? fe.qp : (c < 4 ? fe.kp : fe.vp));
+          ptr = c < 6 ? b16 + row * 2 + (c & 1) * 128 : reinterpret_cast<const char*>(fe.z + row) + (c - 6) * 256;
+        } else {
+          const char* b16 = reinterpret_cast<const char*>(c < 2 ? q : (c < 4 ? k : v));
+          ptr = c < 6 ? b16 + row * 2 + (c & 1) * 128 : reinterpret_cast<const char*>(g + row) + (c - 6) * 256;
+        }
+        prefetch_l2(ptr);
+        if (c >= 6) prefetch_l2(ptr + 128);
+      }
+      if constexpr (kFront) {
+        if (fe.W > 1) {  // the convolution cache of (nb, nh): 3 (W - 1) rows of 512 bytes
+          const char* cb = reinterpret_cast<const char*>(fe.conv_cache + (static_cast<int64_t>(nb) * H + nh) * 3 * (fe.W - 1) * kD);
+          for (int e = lane; e < 3 * (fe.W - 1) * 4; e += 32) prefetch_l2(cb + e * 128);
+        }
+      }
+    }
+  }
   if (nc == 0 && commit_ok && Sout && Sout != Sin) {  // no token committed: the destination takes the entry state
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) __stcs(&Sout[((r0 + 8 * m) * kD + col) >> 2], s[m]);
@@ -355,6 +402,18 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
   }
 }
 
+// The distance of the prefetch in CTAs: half the CTAs resident at once (two per SM).
+// Measured on a GB300 with the state prefetch alone (256 x 96 decode / 4-token verify / paged
+// decode): 1 x SMs 463 / 612 / 513 us, 2 x SMs 465 / 614 / 515, 3 x 494 / 625 / 543, 4 x 563 /
+// 646 / 611, none 485 / 698 / 555 (a longer distance evicts prefetched states before their CTA
+// starts); with the inputs prefetched too, SMs / 2 slows the paged decode (552 vs 503 us).
+int lookahead_ctas() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, float* S,
@@ -364,7 +423,8 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const flo
   if (units == 0) return cudaSuccess;
   decode_kernel<false><<<static_cast<unsigned>(units), kThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), g, beta, S, n_commit, o, n_tok, H, status, pages, FrontEnd());
+      static_cast<const __nv_bfloat16*>(v), g, beta, S, n_commit, o, n_tok, H, status, pages, FrontEnd(),
+      lookahead_ctas());
   return cudaGetLastError();
 }
 
@@ -373,7 +433,8 @@ cudaError_t launch_decode_fused(const FrontEnd& fe, float* S, const int32_t* n_c
   const int64_t units = static_cast<int64_t>(B) * H;
   if (units == 0) return cudaSuccess;
   decode_kernel<true><<<static_cast<unsigned>(units), kThreads, 0, stream>>>(
-      nullptr, nullptr, nullptr, nullptr, nullptr, S, n_commit, o, n_tok, H, status, PageTables(), fe);
+      nullptr, nullptr, nullptr, nullptr, nullptr, S, n_commit, o, n_tok, H, status, PageTables(), fe,
+      lookahead_ctas());
   return cudaGetLastError();
 }
 

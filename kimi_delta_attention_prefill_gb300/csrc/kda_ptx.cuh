@@ -96,6 +96,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1
 }
 
 // Pull the cache line holding `ptr` into L2 (no register result, no completion tracking).
+// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.L2 [%0];\n" ::"l"(reinterpret_cast<uint64_t>(ptr)));
 }
