@@ -48,10 +48,10 @@ PREFILL_TRAFFIC = 1_197_215_488  # 8192 x 96 prefill launch
 GATED_TRAFFIC = 1_401_074_176    # the same with the fused output stage
 SPLIT_1M_TRAFFIC = 23_920_108_800  # 2^20 x 8 split prefill: both prefill passes together
 VARLEN_TRAFFIC = 98_669_809_408   # varlen workload launch
-DECODE_TRAFFIC = None  # 256 x 96 decode launch, one token
-VERIFY_TRAFFIC = {}  # plain verify, n_tok -> bytes
-PAGED_DECODE_TRAFFIC = None  # 256 x 96 decode from scattered pages (page check kernels not included)
-FUSED_TRAFFIC = None  # 256 x 96 fused verify launch
+DECODE_TRAFFIC = 3_207_065_856  # 256 x 96 decode launch, one token
+VERIFY_TRAFFIC = {1: 3_207_065_856, 2: 3_252_792_576, 3: 3_297_135_104, 4: 3_341_306_368}  # plain verify, n_tok
+PAGED_DECODE_TRAFFIC = 3_216_165_632  # 256 x 96 decode from scattered pages (page check kernels not included)
+FUSED_TRAFFIC = 3_298_197_760  # 256 x 96 fused verify launch
 
 
 def load_peaks():
