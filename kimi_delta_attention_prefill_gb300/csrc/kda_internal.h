@@ -99,28 +99,49 @@ struct PrefillArgs {
 // Planner rule ("部署 Kimi K3 ..." section 1.2: split a sequence over the SMs when its
 // rank holds few heads).  A function of the sequence's own length, H, the SM count and
 // the caller's request only, so a sequence is split the same way packed or alone.
-//   n_segments > 0 : min(n_segments, chunks)
-//   n_segments = 0 : the count with the least chain time in a wave model: with n segments
-//     pass 1 runs H (2n - 3) work items and pass 3 H (n - 1), each 1/n of the sequence's
-//     chain, so the time is (ceil(H (2n - 3) / S) + ceil(H (n - 1) / S)) / n of the
-//     unsplit chain (S = SMs, one CTA each); n = 1 costs 1 and ties keep the smaller n.
-//     Candidates: n <= S / H + 1 and n <= chunks / kMinSegChunks.
+//   n_segments > 0 : min(n_segments, chunks) segments of equal length
+//   n_segments = 0 : the count with the least chain time in a wave model (one CTA per SM,
+//     S SMs): with n segments pass 1 runs the first segment and two state-only items per
+//     middle segment, H (2n - 3) items in w1 = ceil(H (2n - 3) / S) waves, and pass 3 the
+//     n - 1 later segments, H (n - 1) items in w3 waves.  The first segment, which needs no
+//     state-only items, is made w1 times as long as the others (it runs through all of
+//     pass 1's waves, launched first), so a segment is 1 / (n - 1 + w1) of the chain and the
+//     time is (w1 + w3) / (n - 1 + w1) of the unsplit chain; n = 1 costs 1 and ties keep the
+//     smaller n.  Candidates: n <= S / H + 1, and segments of at least kMinSegChunks chunks.
 constexpr int kMinSegChunks = 64;  // segments shorter than 4096 tokens do not pay for the extra passes
+
+// Pass 1's waves for n segments (1 when there are no middle segments).
+__host__ __device__ inline int split_pass1_waves(int n, int H, int num_sms) {
+  if (n < 3) return 1;
+  const int64_t h = H > 0 ? H : 1, S = num_sms > 0 ? num_sms : 1;
+  return static_cast<int>((h * (2 * n - 3) + S - 1) / S);
+}
 
 __host__ __device__ inline int plan_segments(int len, int H, int num_sms, int n_segments) {
   const int nch = (len + kChunk - 1) / kChunk;
   if (nch <= 1) return 1;
   if (n_segments > 0) return n_segments < nch ? n_segments : nch;
   const int h = H > 0 ? H : 1, S = num_sms > 0 ? num_sms : 1;
-  int nmax = S / h + 1;
-  if (nch / kMinSegChunks < nmax) nmax = nch / kMinSegChunks;
+  const int nmax = S / h + 1;
   int best = 1;
   int64_t best_w = 1, best_n = 1;  // cost best_w / best_n, compared as cross products
   for (int n = 2; n <= nmax; ++n) {
-    const int64_t w = (static_cast<int64_t>(h) * (2 * n - 3) + S - 1) / S + (static_cast<int64_t>(h) * (n - 1) + S - 1) / S;
-    if (w * best_n < best_w * n) { best = n; best_w = w; best_n = n; }
+    const int w1 = split_pass1_waves(n, h, S);
+    const int64_t parts = n - 1 + w1;  // the chain in parts of one later segment each
+    if (parts * kMinSegChunks > nch) break;
+    const int64_t w = w1 + (static_cast<int64_t>(h) * (n - 1) + S - 1) / S;
+    if (w * best_n < best_w * parts) { best = n; best_w = w; best_n = parts; }
   }
   return best;
+}
+
+// Chunk boundary k (0 <= k <= ns) of a sequence of nch chunks split into ns segments; the
+// first segment has weight w0 (split_pass1_waves for the planner's own count, 1 when the
+// caller forces the count), the others weight 1.
+__host__ __device__ inline int segment_boundary(int k, int ns, int nch, int w0) {
+  if (k <= 0) return 0;
+  const int64_t parts = ns - 1 + w0;
+  return static_cast<int>(((w0 + k - 1) * static_cast<int64_t>(nch)) / parts);
 }
 
 // Work-item modes of the prefill kernel.

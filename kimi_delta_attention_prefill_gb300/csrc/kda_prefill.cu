@@ -159,6 +159,7 @@ struct KParams {
   const int4* items;      // work items (split path) or nullptr: item x = whole sequence x
   const int* item_count;  // device count of valid items
   float* slots;           // split-path state slots [slot][H][3][128][128]
+  int head_in_x;          // items path: grid (H, items), heads first in launch order
   float* pair_S;          // pair mode (no items): S~ of block 2 s, [n_seq][H][128][128]
   float* pair_M;          //                      M  of block 2 s + 1, same layout
 };
@@ -1145,9 +1146,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   // ---- work item: (sequence, head, chunk range, mode)
   int4 it;
+  const int bx = p.head_in_x ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
   if (p.items) {
-    if (static_cast<int>(blockIdx.x) >= *p.item_count) return;
-    it = p.items[blockIdx.x];
+    if (bx >= *p.item_count) return;
+    it = p.items[bx];
   } else if (p.pair_S) {  // pair mode: blocks 2 s and 2 s + 1 give S~ and M of sequence s
     it = make_int4(static_cast<int>(blockIdx.x >> 1), 0, -1, (blockIdx.x & 1) ? kModeTrans : kModeZero);
   } else {
@@ -1156,7 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int mode = it.w & 7, slot = it.w >> 3;
   Work w;
   w.seq = it.x;
-  w.h = blockIdx.y;
+  w.h = p.head_in_x ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
   if (p.pg.fail && *p.pg.fail) return;  // the page check refused the call: nothing is written
   if (tid == 0) {
     int64_t bos; int len, cb, ce;
@@ -1347,12 +1349,19 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.slots = reinterpret_cast<float*>(ws + L.off_slots);
   p.items = reinterpret_cast<const int4*>(ws + L.off_items1);
   p.item_count = reinterpret_cast<const int*>(ws);
-  kernel<<<dim3(static_cast<unsigned>(L.max1), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
+  // heads first in launch order, so every head's first segment (the longest: it runs through
+  // all of pass 1's waves) starts in the first wave; the other order past the grid's y limit
+  auto grid = [&](int64_t items) {
+    p.head_in_x = items <= 65535 ? 1 : 0;
+    return p.head_in_x ? dim3(static_cast<unsigned>(a.H), static_cast<unsigned>(items))
+                       : dim3(static_cast<unsigned>(items), static_cast<unsigned>(a.H));
+  };
+  kernel<<<grid(L.max1), kThreads, kSmemAlloc, a.stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_split_scan(a, L)) != cudaSuccess) return e;
   p.items = reinterpret_cast<const int4*>(ws + L.off_items3);
   p.item_count = reinterpret_cast<const int*>(ws) + 1;
-  kernel<<<dim3(static_cast<unsigned>(L.max3), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
+  kernel<<<grid(L.max3), kThreads, kSmemAlloc, a.stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -58,7 +58,8 @@ __global__ void split_plan_kernel(const int32_t* __restrict__ cu, int n_seq, int
     }
     const int base = static_cast<int>(slot);
     slot += ns;
-    auto cb = [&](int k) { return static_cast<int>((static_cast<int64_t>(k) * nch) / ns); };
+    const int w0 = n_segments > 0 ? 1 : split_pass1_waves(ns, H, num_sms);
+    auto cb = [&](int k) { return segment_boundary(k, ns, nch, w0); };
     items1[n1++] = make_int4(s, 0, cb(1), kModeFirst | (base << 3));
     for (int k = 1; k + 1 < ns; ++k) {
       items1[n1++] = make_int4(s, cb(k), cb(k + 1), kModeZero | ((base + k) << 3));

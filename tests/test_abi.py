@@ -153,12 +153,14 @@ def _split_bytes(n_seq, H, extra):
 
 
 def test_planner_wave_model(lib):
-    """The automatic segment count minimises (ceil(H(2n-3)/S) + ceil(H(n-1)/S)) / n with
-    S = 152 (the library's assumption without a GPU); worked by hand:
-    H = 8, 2^20 tokens: n = 20 (pass 1: 296 items = 2 waves, pass 3: 152 = 1 wave, 3/20);
-    n = 19 would give 3/19 and n = 21 5/21.  H = 16: n = 10 (272 and 144 items, 3/10; 9 gives
-    3/9).  One head, 9000 tokens: at most 2 segments by length, and 2 segments cost 2/2 = 1,
-    a tie with no split, which the planner keeps."""
+    """The automatic segment count minimises (w1 + w3) / (n - 1 + w1), w1 = ceil(H(2n-3)/S)
+    pass-1 waves (the first segment, w1 times as long as the others, runs through all of
+    them) and w3 = ceil(H(n-1)/S) pass-3 waves, with S = 152 (the library's assumption
+    without a GPU); worked by hand:
+    H = 8, 2^20 tokens: n = 20 (pass 1: 296 items = 2 waves, pass 3: 152 = 1 wave, 3/21);
+    n = 19 would give 3/20 and n = 21 (3 + 2)/23.  H = 16: n = 10 (272 and 144 items, 3/11;
+    9 gives 3/10).  One head, 9000 tokens: at most 2 segments by length, and 2 segments cost
+    2/2 = 1, a tie with no split, which the planner keeps."""
     assert kda.prefill_workspace_size(1, 8, 1 << 20) == _split_bytes(1, 8, 19)
     assert kda.prefill_workspace_size(1, 16, 1 << 20) == _split_bytes(1, 16, 9)
     assert kda.prefill_workspace_size(1, 1, 9000) == 0
