@@ -64,8 +64,9 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kRThreads = 128;  // recurrent group: warps 0-3 (TMEM lane quarters 0-3)
 constexpr int kPThreads = 256;  // prep group: warps 4-11
-constexpr uint32_t kBarR = 1, kBarP = 2, kBarXU = 3, kBarL = 4;  // named barrier ids (kBarXU: recurrent
-                                                              // warps 0-1; kBarL: the prep warps that read L)
+// named barrier ids (kBarXU: recurrent warps 0-1; kBarL: the prep warps that read L; kBarO:
+// recurrent warps 2-3, the output rows)
+constexpr uint32_t kBarR = 1, kBarP = 2, kBarXU = 3, kBarL = 4, kBarO = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Block totals table: [4 blocks][16 channel groups], 12 floats per group (8 used), so the
@@ -87,8 +88,11 @@ __host__ __device__ constexpr uint32_t lm_col(int tb) { return tb == 0 ? 0u : tb
 constexpr uint32_t SM_S16 = 0;        // S fp16, [i][j], 2 N-panels x 128 rows        (recurrent)
 constexpr uint32_t SM_KQ = 32768;     // [-K_decay; Q_decay] fp16, K-major, 2 x 128 rows (prep -> recurrent)
 constexpr uint32_t SM_V = 65536;      // v tile (TMA), 16 KiB, one stage                 (recurrent)
-constexpr uint32_t SM_FREE = 81920;   // 16 KiB unused
+constexpr uint32_t SM_OST = 81920;    // o tile of a full chunk, bf16, 2 panels x 64 rows, staged for
+                                      // whole-row stores (recurrent)
 constexpr uint32_t SM_XU = 98304;     // X fp16 [t][j], 2 N-panels x 64 rows             (recurrent)
+                                      // (after the chunk's products: a 32-column slice of a
+                                      // checkpoint or final state, fp32, staged for its stores)
 constexpr uint32_t SM_KR = 114688;    // K_restore, then K_w, fp16 [t][i], 2 panels x 64 (prep -> recurrent)
 constexpr uint32_t SM_IM = 131072;    // [INV Diag(beta); M_qk, then A_o] fp16, 128 rows (prep -> recurrent)
 constexpr uint32_t SM_QAKA = 147456;  // [QA; KA] bf16, K-major, 2 x 128 rows            (prep)
@@ -775,7 +779,7 @@ __device__ __forceinline__ void sigmoid_w_half2(const uint4& a8, const uint32_t 
 // 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (X, then K_w)
 // belong to warps 0-1, rows 64-127 (Q_decay S, then O) to warps 2-3; the state TS uses
 // all 128 lanes.
-template <bool kHook>
+template <bool kHook, bool kGated>
 __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                                 uint32_t tmem, int n_chunks, bool do_o, bool v_zero, bool entry_identity, int tid) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory");
@@ -796,7 +800,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   const uint32_t id_v = idesc_f16(128, 128, true, false, true);
   const float* alast = reinterpret_cast<const float*>(sm + SM_AL);
   const int i = tid;  // state row owned by this thread
-  const bool gated = p.gate != nullptr && do_o;  // output stage on the o rows
+  const bool gated = kGated && do_o;  // output stage on the o rows (the gated instance has p.gate set)
 
   // entry state -> TMEM (fp32) and the fp16 operand copy
 #pragma unroll
@@ -1034,6 +1038,36 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
         ++ck;
       }
       float* fin = (n + 1 == n_chunks) ? w.s_out : nullptr;
+      if (ckdst || fin) {
+        // A checkpoint or the final state, before the decay: each 32-column slice goes through
+        // X's buffer (free until the next chunk's X readout) and is written back as whole
+        // 128-byte lines, a warp storing four rows' slices per instruction, instead of one
+        // 512-byte row per thread.
+        uint8_t* sp = sm + SM_XU;
+        const int rb = (tid >> 5) * 32 + ((tid & 31) >> 3), lc = tid & 7;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          float r[32];
+          tmem_ld32(tmem + tl + kTS + g * 32, r);
+          if (g > 0) named_bar_sync(kBarR, kRThreads);  // the previous slice has been read back
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st4(sp + sw128(i, 16 * c), __float_as_uint(r[4 * c]), __float_as_uint(r[4 * c + 1]),
+                __float_as_uint(r[4 * c + 2]), __float_as_uint(r[4 * c + 3]));
+          named_bar_sync(kBarR, kRThreads);
+          // row rb + 4 j of the slice: 4 rows further is 128 uint4 further
+          uint4* d0 = ckdst ? reinterpret_cast<uint4*>(ckdst + rb * kHeadDim + 32 * g + 4 * lc) : nullptr;
+          uint4* d1 = fin ? reinterpret_cast<uint4*>(fin + rb * kHeadDim + 32 * g + 4 * lc) : nullptr;
+#pragma unroll 2
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sp + sw128(rb + 4 * j, 16 * lc));
+            if (d0) d0[128 * j] = v;
+            if (d1) d1[128 * j] = v;
+          }
+        }
+        ckdst = nullptr;
+        fin = nullptr;
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         float r[32];
@@ -1066,8 +1100,24 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       }
       tmem_wait_st();
     }
-    // ---- outputs (rows in lanes 64-127)
-    if (do_o && rw >= 2 && !gated) {
+    // ---- outputs (rows in lanes 64-127).  A full chunk's rows (o, or y with the output
+    //      stage) are staged in shared memory and written back as whole rows, a warp storing
+    //      two 256-byte rows per instruction, instead of one row per thread; the last,
+    //      partial chunk of a sequence is stored row by row.
+    if (do_o && rw >= 2 && !gated && valid == kChunk) {
+      const int t = tid - 64;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float r[32];
+        tmem_ld32(tmem + tl + kTR1 + g * 32, r);
+        uint8_t* op = sm + SM_OST + (g >> 1) * 8192;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st4(op + sw128(t, 64 * (g & 1) + 16 * c), pack_bf162(r[8 * c], r[8 * c + 1]),
+              pack_bf162(r[8 * c + 2], r[8 * c + 3]), pack_bf162(r[8 * c + 4], r[8 * c + 5]),
+              pack_bf162(r[8 * c + 6], r[8 * c + 7]));
+      }
+    } else if (do_o && rw >= 2 && !gated) {
       const int t = tid - 64;
       const bool wr = t < valid;
       __nv_bfloat16* orow = p.o + ((row0 + t) * p.H + w.h) * kHeadDim;
@@ -1110,7 +1160,13 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
           float r[16];
           tmem_ld16(tmem + tl + kTR1 + g * 32 + 16 * h, r);
           if (wr) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + g * 32 + 16 * h);
+            // staged: the two 16-byte pieces of columns 16 (2 g + h) .. + 15 sit at
+            // sw128(t, 32 (2 g + h) + 16 c), i.e. a swizzled pair base, piece c ^ (t & 1)
+            const bool st = valid == kChunk;
+            uint4* dst = st ? reinterpret_cast<uint4*>(sm + SM_OST + (g >> 1) * 8192 + t * 128 +
+                                                       (((4 * (g & 1) + 2 * h) ^ (t & 6)) << 4))
+                            : reinterpret_cast<uint4*>(orow + g * 32 + 16 * h);
+            const int cx = st ? (t & 1) : 0;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               float y[8];
@@ -1123,12 +1179,24 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
                 y[2 * e] = v.x;
                 y[2 * e + 1] = v.y;
               }
-              dst[c] = make_uint4(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]), pack_bf162(y[4], y[5]),
-                                  pack_bf162(y[6], y[7]));
+              dst[c ^ cx] = make_uint4(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]), pack_bf162(y[4], y[5]),
+                                       pack_bf162(y[6], y[7]));
             }
           }
         }
       }
+    }
+    if (do_o && rw >= 2 && valid == kChunk) {
+      const int t = tid - 64;
+      named_bar_sync(kBarO, 64);
+      // lane: 16-byte column piece oc of row 2 j + (lane / 16) of this warp's 32 rows
+      const int ob = (t >> 5) * 32 + ((t & 31) >> 4), oc = t & 15;
+      const int64_t rs2 = 2 * static_cast<int64_t>(p.H) * kHeadDim;  // two rows of o
+      __nv_bfloat16* od = p.o + ((row0 + ob) * p.H + w.h) * kHeadDim + 8 * oc;
+      const uint8_t* os = sm + SM_OST + (oc >> 3) * 8192;
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j, od += rs2)
+        *reinterpret_cast<uint4*>(od) = *reinterpret_cast<const uint4*>(os + sw128(ob + 2 * j, 16 * (oc & 7)));
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -1136,7 +1204,8 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   }
 }
 
-template <bool kHook>
+// Instances: kHook (the test hook's short waits) x kGated (the output stage fused).
+template <bool kHook, bool kGated>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1228,7 +1297,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int n_chunks = w.c1 - w.c0;
 
   if (tid < kRThreads)
-    recurrent_group<kHook>(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
+    recurrent_group<kHook, kGated>(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
   else
     prep_group<kHook>(p, w, sm, bars, ctrl, tmem, n_chunks, tid - kRThreads);
 
@@ -1253,9 +1322,10 @@ cudaError_t set_smem_attr() {
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
   if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e = cudaSuccess;
+    for (auto k : {prefill_kernel<false, false>, prefill_kernel<false, true>, prefill_kernel<true, false>,
+                   prefill_kernel<true, true>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
@@ -1307,8 +1377,8 @@ cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde)
   p.pair_S = S_tilde; p.pair_M = M;
   cudaError_t e = set_smem_attr();
   if (e != cudaSuccess) return e;
-  prefill_kernel<false><<<dim3(2u * static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc,
-                          a.stream>>>(p);
+  prefill_kernel<false, false><<<dim3(2u * static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads,
+                                 kSmemAlloc, a.stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1335,7 +1405,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   cudaError_t e0 = set_smem_attr();
   if (e0 != cudaSuccess) return e0;
   // the test hook's instance only when kda_debug_stall_next_prefill armed this launch
-  auto kernel = a.stall_chunk >= 0 ? prefill_kernel<true> : prefill_kernel<false>;
+  auto kernel = a.gate ? (a.stall_chunk >= 0 ? prefill_kernel<true, true> : prefill_kernel<false, true>)
+                       : (a.stall_chunk >= 0 ? prefill_kernel<true, false> : prefill_kernel<false, false>);
   const SplitLayout L = split_layout(a.n_seq, a.H, T, a.n_segments, num_sms);
   if (L.extra == 0) {
     // one CTA per (sequence, head), whole sequence
