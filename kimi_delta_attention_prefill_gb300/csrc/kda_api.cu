@@ -291,12 +291,13 @@ kda_status kda_prefill_pairs(const kda_bf16* q, const kda_bf16* k, const kda_bf1
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(M, 16) ||
       !aligned(S_tilde, 16) || !aligned(beta, 4) || !aligned(cu_seqlens, 4) || !aligned(dev_status, 4))
     return KDA_ERR_ALIGNMENT;
-  kda_status st = current_device(nullptr);
+  int sms = 0;
+  kda_status st = current_device(&sms);
   if (st != KDA_OK) return st;
   kda::PrefillArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens; a.n_seq = n_seq;
   a.total_tokens = total_tokens; a.H = H; a.status = dev_status; a.stream = stream;
-  cudaError_t e = kda::launch_prefill_pairs(a, M, S_tilde);
+  cudaError_t e = kda::launch_prefill_pairs(a, M, S_tilde, sms);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

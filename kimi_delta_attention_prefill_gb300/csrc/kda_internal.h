@@ -202,7 +202,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms);
 
 // Pair mode of the prefill kernel: per (sequence, head) the zero-entry state S~ and the
 // transition M of the sequence's rows, into [n_seq][H][128][128] each.
-cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde);
+cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde, int num_sms);
 // entry = fold over r < n_pairs of E <- S~_r + M_r E, from E = S_in (zeros when null).
 cudaError_t launch_combine_pairs(const float* M, const float* S_tilde, int n_pairs, const float* S_in, float* entry,
                                  int n_seq, int H, cudaStream_t stream);

@@ -779,7 +779,7 @@ __device__ __forceinline__ void sigmoid_w_half2(const uint4& a8, const uint32_t 
 // 128 threads; thread = TMEM lane (warp = lane quarter).  Rows 0-63 of TR1 (X, then K_w)
 // belong to warps 0-1, rows 64-127 (Q_decay S, then O) to warps 2-3; the state TS uses
 // all 128 lanes.
-template <bool kHook, bool kGated>
+template <bool kHook, bool kGated, bool kCompact>
 __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, uint64_t* bars, volatile int* ctrl,
                                 uint32_t tmem, int n_chunks, bool do_o, bool v_zero, bool entry_identity, int tid) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory");
@@ -801,6 +801,12 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   const float* alast = reinterpret_cast<const float*>(sm + SM_AL);
   const int i = tid;  // state row owned by this thread
   const bool gated = kGated && do_o;  // output stage on the o rows (the gated instance has p.gate set)
+  // The compact instance keeps the 32-column readout loops rolled: when every SM runs this
+  // kernel, instruction fetch is what the chain waits on, and the smaller loop body wins.
+  constexpr int kRU = kCompact ? 1 : 4;
+  // (the checkpoint / final-state slices the other way round: measured fastest that way in
+  // each instance)
+  constexpr int kSU = kCompact ? 4 : 1;
 
   // entry state -> TMEM (fp32) and the fp16 operand copy
 #pragma unroll
@@ -895,7 +901,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       {
         const int t = tid;
         const bool mk = t < valid;
-#pragma unroll
+#pragma unroll kRU
         for (int g = 0; g < 4; ++g) {
           float r[32];
           tmem_ld32(tmem + tl + kTR1 + g * 32, r);
@@ -942,7 +948,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
       tc_fence_after();
       {
         const int t = tid;  // row of K_w (token s) and of A_o (token t)
-#pragma unroll
+#pragma unroll kRU
         for (int g = 0; g < 4; ++g) {
           float r[32];
           tmem_ld32(tmem + tl + kTR1 + g * 32, r);
@@ -1045,7 +1051,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
         // 512-byte row per thread.
         uint8_t* sp = sm + SM_XU;
         const int rb = (tid >> 5) * 32 + ((tid & 31) >> 3), lc = tid & 7;
-#pragma unroll 1
+#pragma unroll kSU
         for (int g = 0; g < 4; ++g) {
           float r[32];
           tmem_ld32(tmem + tl + kTS + g * 32, r);
@@ -1068,7 +1074,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
         ckdst = nullptr;
         fin = nullptr;
       }
-#pragma unroll
+#pragma unroll kRU
       for (int g = 0; g < 4; ++g) {
         float r[32];
         tmem_ld32(tmem + tl + kTS + g * 32, r);
@@ -1106,7 +1112,7 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
     //      partial chunk of a sequence is stored row by row.
     if (do_o && rw >= 2 && !gated && valid == kChunk) {
       const int t = tid - 64;
-#pragma unroll
+#pragma unroll kRU
       for (int g = 0; g < 4; ++g) {
         float r[32];
         tmem_ld32(tmem + tl + kTR1 + g * 32, r);
@@ -1204,8 +1210,9 @@ __device__ void recurrent_group(const KParams& p, const Work& w, uint8_t* sm, ui
   }
 }
 
-// Instances: kHook (the test hook's short waits) x kGated (the output stage fused).
-template <bool kHook, bool kGated>
+// Instances: kHook (the test hook's short waits), kGated (the output stage fused), kCompact
+// (rolled readout loops, for launches that give every SM a CTA).
+template <bool kHook, bool kGated, bool kCompact>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1297,7 +1304,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int n_chunks = w.c1 - w.c0;
 
   if (tid < kRThreads)
-    recurrent_group<kHook, kGated>(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
+    recurrent_group<kHook, kGated, kCompact>(p, w, sm, bars, ctrl, tmem, n_chunks, do_o, v_zero, entry_identity, tid);
   else
     prep_group<kHook>(p, w, sm, bars, ctrl, tmem, n_chunks, tid - kRThreads);
 
@@ -1323,8 +1330,9 @@ cudaError_t set_smem_attr() {
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
   if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaSuccess;
-    for (auto k : {prefill_kernel<false, false>, prefill_kernel<false, true>, prefill_kernel<true, false>,
-                   prefill_kernel<true, true>})
+    for (auto k : {prefill_kernel<false, false, false>, prefill_kernel<false, false, true>,
+                   prefill_kernel<false, true, false>, prefill_kernel<true, false, false>,
+                   prefill_kernel<true, true, false>})
       if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_release);
@@ -1362,7 +1370,7 @@ bool make_map(CUtensorMap* m, const void* base, bool is_f32, int H, int64_t T) {
 
 }  // namespace
 
-cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde) {
+cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde, int num_sms) {
   KParams p;
   memset(&p, 0, sizeof(p));
   const int64_t T = a.total_tokens;
@@ -1377,8 +1385,10 @@ cudaError_t launch_prefill_pairs(const PrefillArgs& a, float* M, float* S_tilde)
   p.pair_S = S_tilde; p.pair_M = M;
   cudaError_t e = set_smem_attr();
   if (e != cudaSuccess) return e;
-  prefill_kernel<false, false><<<dim3(2u * static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads,
-                                 kSmemAlloc, a.stream>>>(p);
+  const dim3 grid(2u * static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H));
+  auto kernel = static_cast<int64_t>(grid.x) * grid.y >= num_sms ? prefill_kernel<false, false, true>
+                                                                 : prefill_kernel<false, false, false>;
+  kernel<<<grid, kThreads, kSmemAlloc, a.stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1404,10 +1414,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
   p.n_seq = a.n_seq; p.H = a.H; p.total_tokens = T; p.n_ckpt = a.n_ckpt;
   cudaError_t e0 = set_smem_attr();
   if (e0 != cudaSuccess) return e0;
-  // the test hook's instance only when kda_debug_stall_next_prefill armed this launch
-  auto kernel = a.gate ? (a.stall_chunk >= 0 ? prefill_kernel<true, true> : prefill_kernel<false, true>)
-                       : (a.stall_chunk >= 0 ? prefill_kernel<true, false> : prefill_kernel<false, false>);
   const SplitLayout L = split_layout(a.n_seq, a.H, T, a.n_segments, num_sms);
+  // the test hook's instance only when kda_debug_stall_next_prefill armed this launch; the
+  // compact one when every SM gets a CTA (the split passes fill the SMs by construction)
+  const bool full = L.extra > 0 || static_cast<int64_t>(a.n_seq) * a.H >= num_sms;
+  auto kernel = a.gate ? (a.stall_chunk >= 0 ? prefill_kernel<true, true, false> : prefill_kernel<false, true, false>)
+                       : a.stall_chunk >= 0 ? prefill_kernel<true, false, false>
+                       : full ? prefill_kernel<false, false, true>
+                              : prefill_kernel<false, false, false>;
   if (L.extra == 0) {
     // one CTA per (sequence, head), whole sequence
     kernel<<<dim3(static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);

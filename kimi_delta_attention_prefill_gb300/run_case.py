@@ -22,6 +22,7 @@ def main():
     ap.add_argument("--workload", default="prefill_8k", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
     ap.add_argument("--tokens", type=int, default=None, help="override the length of a single-sequence prefill")
+    ap.add_argument("--n-seq", type=int, default=1, help="with --tokens: this many sequences of that length")
     ap.add_argument("--segments", type=int, default=0, help="prefill segment count (0 = library's choice)")
     ap.add_argument("--n-tok", type=int, default=None, help="override the tokens of a decode / verify step")
     ap.add_argument("--iters", type=int, default=3)
@@ -35,7 +36,7 @@ def main():
     if args.heads:
         over["H"] = args.heads
     if args.tokens:
-        over["lengths"] = [args.tokens]
+        over["lengths"] = [args.tokens] * args.n_seq
     if args.n_tok:
         over["n_tok"] = args.n_tok
     x = inputs.make_workload(args.workload, device="cuda", **over)
