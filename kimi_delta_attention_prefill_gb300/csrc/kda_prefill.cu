@@ -163,7 +163,9 @@ struct KParams {
   const int4* items;      // work items (split path) or nullptr: item x = whole sequence x
   const int* item_count;  // device count of valid items
   float* slots;           // split-path state slots [slot][H][3][128][128]
-  int head_in_x;          // items path: grid (H, items), heads first in launch order
+  int head_in_x;          // grid (H, items or ranks): heads first in launch order
+  int lpt;                // plain path, several sequences: grid (H, n_seq), y = the rank of the
+                          // sequence by length, longest first
   float* pair_S;          // pair mode (no items): S~ of block 2 s, [n_seq][H][128][128]
   float* pair_M;          //                      M  of block 2 s + 1, same layout
 };
@@ -206,6 +208,28 @@ __device__ bool check_sequence(const KParams& p, int seq, int64_t& bos, int& len
     }
   }
   return true;
+}
+
+// The sequence of rank `rank` when sequences are ordered by length, longest first (ties by
+// index): the plain launch of several sequences takes them in this order, so the longest
+// units start first and the last wave is made of short ones.  Every thread of the CTA
+// calls this; `scratch` is 2 KB + 4 B of shared memory (n_seq <= 256).
+__device__ int lpt_sequence(const KParams& p, int rank, uint8_t* scratch, int tid, int n_threads) {
+  int32_t* cu = reinterpret_cast<int32_t*>(scratch);
+  int* found = reinterpret_cast<int*>(scratch + 2048);
+  for (int s = tid; s <= p.n_seq; s += n_threads) cu[s] = p.cu[s];
+  __syncthreads();
+  for (int s = tid; s < p.n_seq; s += n_threads) {
+    const int64_t ls = static_cast<int64_t>(cu[s + 1]) - cu[s];
+    int r = 0;
+    for (int t = 0; t < p.n_seq; ++t) {
+      const int64_t lt = static_cast<int64_t>(cu[t + 1]) - cu[t];
+      r += (lt > ls || (lt == ls && t < s)) ? 1 : 0;
+    }
+    if (r == rank) *found = s;  // the ranks are a permutation: exactly one thread writes
+  }
+  __syncthreads();
+  return *found;
 }
 
 // The kernel's waits, all bounded.  The instance kHook (launched only by the test hook
@@ -1228,6 +1252,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     it = p.items[bx];
   } else if (p.pair_S) {  // pair mode: blocks 2 s and 2 s + 1 give S~ and M of sequence s
     it = make_int4(static_cast<int>(blockIdx.x >> 1), 0, -1, (blockIdx.x & 1) ? kModeTrans : kModeZero);
+  } else if (!kGated && p.lpt) {  // the o stage is free before the first chunk: scratch for the ranking
+    it = make_int4(lpt_sequence(p, static_cast<int>(blockIdx.y), sm + SM_OST, tid, kThreads), 0, -1, kModeFull);
   } else {
     it = make_int4(static_cast<int>(blockIdx.x), 0, -1, kModeFull);
   }
@@ -1423,8 +1449,15 @@ cudaError_t launch_prefill(const PrefillArgs& a, int num_sms) {
                        : full ? prefill_kernel<false, false, true>
                               : prefill_kernel<false, false, false>;
   if (L.extra == 0) {
-    // one CTA per (sequence, head), whole sequence
-    kernel<<<dim3(static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
+    // one CTA per (sequence, head), whole sequence; several sequences (up to 256, plain
+    // output) are launched longest first, every head of a sequence together
+    if (a.n_seq > 1 && a.n_seq <= 256 && !a.gate) {
+      p.lpt = 1;
+      p.head_in_x = 1;
+      kernel<<<dim3(static_cast<unsigned>(a.H), static_cast<unsigned>(a.n_seq)), kThreads, kSmemAlloc, a.stream>>>(p);
+    } else {
+      kernel<<<dim3(static_cast<unsigned>(a.n_seq), static_cast<unsigned>(a.H)), kThreads, kSmemAlloc, a.stream>>>(p);
+    }
     return cudaGetLastError();
   }
   // sequence split: plan, pass 1 (first segments + (S~, M) of middle segments), scan, pass 3
