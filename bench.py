@@ -44,10 +44,10 @@ CPU_SAMPLE_TOKENS = 8192  # the whole workload: about 1.5 s on 16 host cores (ab
 # capture of each launch timed here, at the benched shapes and inputs (no scaling); the
 # captures and the commands that made them are summarised in profiles/.  None when the
 # kernel changed after the counters were taken, until it is captured again.
-PREFILL_TRAFFIC = None  # 8192 x 96 prefill launch
-GATED_TRAFFIC = None    # the same with the fused output stage
-SPLIT_1M_TRAFFIC = None  # 2^20 x 8 split prefill: both prefill passes together
-VARLEN_TRAFFIC = None   # varlen workload launch
+PREFILL_TRAFFIC = 1_197_863_168  # 8192 x 96 prefill launch
+GATED_TRAFFIC = 1_401_359_104    # the same with the fused output stage
+SPLIT_1M_TRAFFIC = 24_376_601_344  # 2^20 x 8 split prefill: both prefill passes together
+VARLEN_TRAFFIC = 92_123_368_704   # varlen workload launch
 DECODE_TRAFFIC = 3_207_065_856  # 256 x 96 decode launch, one token
 VERIFY_TRAFFIC = {1: 3_207_065_856, 2: 3_252_792_576, 3: 3_297_135_104, 4: 3_341_306_368}  # plain verify, n_tok
 PAGED_DECODE_TRAFFIC = 3_216_165_632  # 256 x 96 decode from scattered pages (page check kernels not included)
