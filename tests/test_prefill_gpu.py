@@ -358,3 +358,51 @@ def test_large_values_within_the_fp16_operand_range():
     assert st == 0
     assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
     check_against_oracle(inp, o, S, ck)
+
+
+def _packed_equals_standalone(inp, o, S, ck, seqs):
+    cu, off, pos = inp.cu_seqlens.tolist(), inp.ckpt_off.tolist(), inp.ckpt_pos.tolist()
+    for s in seqs:
+        a, b = cu[s], cu[s + 1]
+        one = inputs.PrefillInputs(inp.q[a:b], inp.k[a:b], inp.v[a:b], inp.g[a:b], inp.beta[a:b],
+                                   inp.S0[s:s + 1], torch.tensor([0, b - a], dtype=torch.int32),
+                                   torch.tensor([0, off[s + 1] - off[s]], dtype=torch.int32),
+                                   torch.tensor(pos[off[s]:off[s + 1]], dtype=torch.int32))
+        o1, S1, ck1, st1, _ = run_gpu(one)
+        assert st1 == 0
+        assert torch.equal(o1, o[a:b]) and torch.equal(S1[0], S[s]), f"sequence {s}"
+        if off[s + 1] > off[s]:
+            assert torch.equal(ck1, ck[off[s]:off[s + 1]])
+
+
+def test_full_gpu_packed_launch_longest_first_equals_standalone():
+    """A packed launch with at least one unit per SM (the compact kernel instance, sequences
+    taken longest first, ties by index) against the oracle and, bit for bit, against each
+    sequence run alone (a few units: the full instance, launch order irrelevant)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    n_seq = (sms + H - 1) // H + 2
+    rng = np.random.default_rng(404)
+    lens = rng.integers(1, 700, size=n_seq).tolist()
+    lens[3] = lens[7] = lens[11]  # ties in the ranking
+    inp = inputs.make_prefill(lens, H=H, seed=404, device="cpu", decay="uniform", s0_std=0.02, ckpt_every=64)
+    o, S, ck, st, o_buf = run_gpu(inp, o_pad=64)
+    assert st == 0
+    assert torch.isnan(o_buf[:64].float()).all() and torch.isnan(o_buf[-64:].float()).all()
+    assert not torch.isnan(o.float()).any()
+    units = [(s, h) for s in range(0, n_seq, 5) for h in range(H)]
+    check_against_oracle(inp, o, S, ck, units=units)
+    _packed_equals_standalone(inp, o, S, ck, range(n_seq))
+
+
+def test_more_than_256_sequences_launch_in_index_order():
+    """Past 256 sequences the packed launch keeps the index order (no ranking); results do
+    not depend on it."""
+    n_seq = 257
+    rng = np.random.default_rng(405)
+    lens = rng.integers(1, 140, size=n_seq).tolist()
+    inp = inputs.make_prefill(lens, H=1, seed=405, device="cpu", decay="uniform", s0_std=0.02, ckpt_every=64)
+    o, S, ck, st, _ = run_gpu(inp)
+    assert st == 0
+    check_against_oracle(inp, o, S, ck, units=[(s, 0) for s in range(0, n_seq, 16)])
+    _packed_equals_standalone(inp, o, S, ck, range(0, n_seq, 8))
