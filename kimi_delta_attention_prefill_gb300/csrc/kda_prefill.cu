@@ -44,7 +44,11 @@
 //       the recurrence ("部署 Kimi K3 ..." 1.1: overlap the intra-chunk work with the
 //       inter-chunk state hand-off).
 // The groups hand operands over through shared memory guarded by mbarriers; every wait
-// is bounded and a timeout ends the CTA with KDA_ERR_TIMEOUT.
+// is bounded and a timeout ends the CTA with KDA_ERR_TIMEOUT.  Outputs and states leave
+// through shared memory as whole lines (a thread owns a TMEM row, so its own stores would
+// touch 32 rows per warp instruction).  Instances: the test hook's, the fused output stage,
+// and a compact one (rolled readout loops) for launches that give every SM a CTA, where
+// instruction fetch, not the chain, is what grows.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
