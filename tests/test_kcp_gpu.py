@@ -61,6 +61,25 @@ def test_pairs_against_the_oracle():
     assert torch.equal(St[1], torch.zeros_like(St[1]))
 
 
+def test_pairs_at_full_width_equal_a_narrow_launch_bit_for_bit():
+    """Pair mode with at least one CTA per SM (the compact kernel instance) against the same
+    heads in a narrow launch (the full instance): the same arithmetic, so the same bits."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = (sms + 3) // 4 + 2  # 2 sequences x 2 items x H >= SMs
+    x = inputs.make_prefill([150, 70], H=H, seed=94, device="cpu", decay="uniform")
+    x.g.mul_(0.004)
+    d = to_device(x)
+    M, St = kda.prefill_pairs(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"])
+    narrow = {key: (val[:, :2].contiguous() if key in ("q", "k", "v", "g", "beta") else val) for key, val in d.items()}
+    M2, St2 = kda.prefill_pairs(narrow["q"], narrow["k"], narrow["v"], narrow["g"], narrow["beta"],
+                                narrow["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert torch.equal(M[:, :2], M2) and torch.equal(St[:, :2], St2)
+    ref = oracle_units(x, [(0, H - 1), (1, H - 1)])
+    for s in range(2):
+        assert rel_fro(host(St[s, H - 1]), ref[(s, H - 1)]["S"]) <= S_TOL
+
+
 def test_combine_against_numpy():
     gen = torch.Generator().manual_seed(5)
     R, N, H = 3, 2, 3
