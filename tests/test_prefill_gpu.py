@@ -395,10 +395,11 @@ def test_full_gpu_packed_launch_longest_first_equals_standalone():
     _packed_equals_standalone(inp, o, S, ck, range(n_seq))
 
 
-def test_more_than_256_sequences_launch_in_index_order():
-    """Past 256 sequences the packed launch keeps the index order (no ranking); results do
-    not depend on it."""
-    n_seq = 257
+@pytest.mark.parametrize("n_seq", [256, 257])
+def test_ranking_limit_256_sequences(n_seq):
+    """256 sequences: the largest launch that ranks them by length (each CTA compares 256 x
+    256 lengths); 257: past the limit the packed launch keeps the index order.  Results do
+    not depend on the order."""
     rng = np.random.default_rng(405)
     lens = rng.integers(1, 140, size=n_seq).tolist()
     inp = inputs.make_prefill(lens, H=1, seed=405, device="cpu", decay="uniform", s0_std=0.02, ckpt_every=64)
